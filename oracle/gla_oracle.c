@@ -1,0 +1,314 @@
+/*
+ * gla_oracle.c — plain, slow, fp64 CPU reference for Simple Gated Linear
+ * Attention (Simple GLA).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker the CUDA library is
+ * compared against.  Only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it; the library never links, calls or falls back
+ * to it, and it shares no code, header or table with the CUDA path.
+ *
+ * Citation key used below:
+ *   [L3B]  the page "线性注意力模型如何实现固定推理状态" (Beyond the KV cache:
+ *          training and serving i14's Laplace 3B linear attention model on AWS
+ *          Trainium2).  Sections: "i14 与 Laplace 3B 架构" (GLA mixer: state
+ *          update, state read-out, decay scheme) and "挑战 1" (chunked GLA:
+ *          intra-chunk output and chunk state update, Figure 3).
+ *   [RFB]  the blog page on recurrence-free pre-trained recurrent networks,
+ *          §3.2 (the state update S_t = S_{t-1} + k_t v_t as a prefix sum).
+ *
+ * The formula images on [L3B] did not survive extraction; only their captions
+ * and the surrounding prose did.  The readings taken here:
+ *   - per head h a fixed scalar decay lambda_h = exp(log_decay[h]) in (0, 1];
+ *   - state S (dk x dv) updated as  S_t = lambda * S_{t-1} + k_t^T v_t;
+ *   - read-out after the update:     o_t = q_t S_t   (no extra scale);
+ *   - chunk c of length L (local positions i, j):
+ *       O_c = ((Q_c K_c^T) .* D) V_c + diag(lambda^(i+1)) Q_c S_{c-1},
+ *             D_ij = lambda^(i-j) for j <= i, else 0
+ *       S_c = lambda^L S_{c-1} + K_c^T diag(lambda^(L-1-j)) V_c.
+ *
+ * Layout (row-major, innermost last):
+ *   q, k : [rows, H, dk]   float32 (exact copies of bf16 / fp32 inputs)
+ *   v    : [rows, H, dv]   float32
+ *   o    : [rows, H, dv]   float64 (written)
+ *   h0,hT: [nseq, H, dk, dv] float64 (h0 may be NULL = zeros; hT may be NULL)
+ * A sequence s occupies rows seq_start[s] .. seq_start[s]+seq_len[s]-1.  A
+ * dense batch [B, T, ...] is the case seq_start[b] = b*T, seq_len[b] = T.
+ *
+ * units: optional list of (sequence, head) pairs (2*nunits int32) selecting
+ * which chains to compute; NULL computes every chain.  Rows of o that belong to
+ * chains not selected are left untouched.
+ *
+ * All entry points return 0 on success and -1 on a bad argument.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    const float *q, *k, *v;
+    const double *log_decay;
+    const double *h0;
+    double *o, *hT;
+    const int64_t *seq_start, *seq_len;
+    int nseq, H, dk, dv;
+    const int32_t *units;
+    int nunits;
+    int chunk;       /* used by the chunked form only */
+    int form;        /* 0 recurrent, 1 quadratic, 2 chunked */
+    int next_unit;   /* shared work counter */
+    int error;
+} job_t;
+
+/* lambda^n for integer n >= 0, from the natural-log decay. */
+static double decay_pow(double log_decay, double n) { return exp(n * log_decay); }
+
+/*
+ * Token-by-token recurrence for one (sequence, head) chain.
+ * [L3B] §"i14 与 Laplace 3B 架构", GLA mixer: the per-token state update and
+ * the state read-out.
+ */
+static void chain_recurrent(const job_t *J, int s, int h) {
+    const int H = J->H, dk = J->dk, dv = J->dv;
+    const double lam = exp(J->log_decay[h]);
+    double *S = (double *)calloc((size_t)dk * dv, sizeof(double));
+    if (J->h0) memcpy(S, J->h0 + ((size_t)s * H + h) * dk * dv, sizeof(double) * dk * dv);
+    for (int64_t t = 0; t < J->seq_len[s]; ++t) {
+        const int64_t row = J->seq_start[s] + t;
+        const float *qt = J->q + ((size_t)row * H + h) * dk;
+        const float *kt = J->k + ((size_t)row * H + h) * dk;
+        const float *vt = J->v + ((size_t)row * H + h) * dv;
+        double *ot = J->o + ((size_t)row * H + h) * dv;
+        for (int j = 0; j < dv; ++j) ot[j] = 0.0;
+        for (int i = 0; i < dk; ++i) {
+            double *Si = S + (size_t)i * dv;
+            const double ki = kt[i], qi = qt[i];
+            for (int j = 0; j < dv; ++j) {
+                Si[j] = lam * Si[j] + ki * (double)vt[j];   /* S_t = lam S_{t-1} + k_t^T v_t */
+                ot[j] += qi * Si[j];                        /* o_t = q_t S_t                 */
+            }
+        }
+    }
+    if (J->hT) memcpy(J->hT + ((size_t)s * H + h) * dk * dv, S, sizeof(double) * dk * dv);
+    free(S);
+}
+
+/*
+ * Quadratic (attention) form of the same map for one chain:
+ *   o_i = sum_{j<=i} lambda^(i-j) (q_i . k_j) v_j + lambda^(i+1) q_i S_0
+ *   S_T = lambda^T S_0 + sum_j lambda^(T-1-j) k_j^T v_j
+ * Obtained by unrolling the [L3B] GLA-mixer recurrence; used to pin the
+ * recurrence above.  Powers of lambda come from exp(n * log_decay) here, not
+ * from repeated products, so the two forms round differently.
+ */
+static void chain_quadratic(const job_t *J, int s, int h) {
+    const int H = J->H, dk = J->dk, dv = J->dv;
+    const double ld = J->log_decay[h];
+    const int64_t T = J->seq_len[s], r0 = J->seq_start[s];
+    const double *S0 = J->h0 ? J->h0 + ((size_t)s * H + h) * dk * dv : NULL;
+    for (int64_t i = 0; i < T; ++i) {
+        const float *qi = J->q + ((size_t)(r0 + i) * H + h) * dk;
+        double *oi = J->o + ((size_t)(r0 + i) * H + h) * dv;
+        for (int c = 0; c < dv; ++c) oi[c] = 0.0;
+        for (int64_t j = 0; j <= i; ++j) {
+            const float *kj = J->k + ((size_t)(r0 + j) * H + h) * dk;
+            const float *vj = J->v + ((size_t)(r0 + j) * H + h) * dv;
+            double a = 0.0;
+            for (int d = 0; d < dk; ++d) a += (double)qi[d] * (double)kj[d];
+            a *= decay_pow(ld, (double)(i - j));
+            for (int c = 0; c < dv; ++c) oi[c] += a * (double)vj[c];
+        }
+        if (S0) {
+            const double g = decay_pow(ld, (double)(i + 1));
+            for (int d = 0; d < dk; ++d)
+                for (int c = 0; c < dv; ++c) oi[c] += g * (double)qi[d] * S0[(size_t)d * dv + c];
+        }
+    }
+    if (J->hT) {
+        double *ST = J->hT + ((size_t)s * H + h) * dk * dv;
+        const double gT = decay_pow(ld, (double)T);
+        for (size_t e = 0; e < (size_t)dk * dv; ++e) ST[e] = S0 ? gT * S0[e] : 0.0;
+        for (int64_t j = 0; j < T; ++j) {
+            const float *kj = J->k + ((size_t)(r0 + j) * H + h) * dk;
+            const float *vj = J->v + ((size_t)(r0 + j) * H + h) * dv;
+            const double g = decay_pow(ld, (double)(T - 1 - j));
+            for (int d = 0; d < dk; ++d)
+                for (int c = 0; c < dv; ++c) ST[(size_t)d * dv + c] += g * (double)kj[d] * (double)vj[c];
+        }
+    }
+}
+
+/*
+ * Chunkwise form for one chain, chunk length C (the last chunk may be shorter).
+ * [L3B] §"挑战 1": intra-chunk output = decay-masked linear attention plus the
+ * carried state's contribution; then the chunk state update with the decay
+ * accumulated over the chunk (Figure 3).  Used only to check that the chunked
+ * and recurrent forms agree.
+ */
+static void chain_chunked(const job_t *J, int s, int h) {
+    const int H = J->H, dk = J->dk, dv = J->dv, C = J->chunk;
+    const double ld = J->log_decay[h];
+    const int64_t T = J->seq_len[s], r0 = J->seq_start[s];
+    double *S = (double *)calloc((size_t)dk * dv, sizeof(double));
+    double *dS = (double *)calloc((size_t)dk * dv, sizeof(double));
+    if (J->h0) memcpy(S, J->h0 + ((size_t)s * H + h) * dk * dv, sizeof(double) * dk * dv);
+    for (int64_t c0 = 0; c0 < T; c0 += C) {
+        const int64_t L = (T - c0 < C) ? (T - c0) : C;
+        /* output of the chunk, using S = S_{c-1} */
+        for (int64_t i = 0; i < L; ++i) {
+            const float *qi = J->q + ((size_t)(r0 + c0 + i) * H + h) * dk;
+            double *oi = J->o + ((size_t)(r0 + c0 + i) * H + h) * dv;
+            for (int c = 0; c < dv; ++c) oi[c] = 0.0;
+            for (int64_t j = 0; j <= i; ++j) {            /* ((Q K^T) .* D) V */
+                const float *kj = J->k + ((size_t)(r0 + c0 + j) * H + h) * dk;
+                const float *vj = J->v + ((size_t)(r0 + c0 + j) * H + h) * dv;
+                double a = 0.0;
+                for (int d = 0; d < dk; ++d) a += (double)qi[d] * (double)kj[d];
+                a *= decay_pow(ld, (double)(i - j));
+                for (int c = 0; c < dv; ++c) oi[c] += a * (double)vj[c];
+            }
+            const double g = decay_pow(ld, (double)(i + 1));   /* diag(lambda^(i+1)) Q S */
+            for (int d = 0; d < dk; ++d)
+                for (int c = 0; c < dv; ++c) oi[c] += g * (double)qi[d] * S[(size_t)d * dv + c];
+        }
+        /* S_c = lambda^L S_{c-1} + K^T diag(lambda^(L-1-j)) V */
+        memset(dS, 0, sizeof(double) * dk * dv);
+        for (int64_t j = 0; j < L; ++j) {
+            const float *kj = J->k + ((size_t)(r0 + c0 + j) * H + h) * dk;
+            const float *vj = J->v + ((size_t)(r0 + c0 + j) * H + h) * dv;
+            const double g = decay_pow(ld, (double)(L - 1 - j));
+            for (int d = 0; d < dk; ++d)
+                for (int c = 0; c < dv; ++c) dS[(size_t)d * dv + c] += (double)kj[d] * g * (double)vj[c];
+        }
+        const double gL = decay_pow(ld, (double)L);
+        for (size_t e = 0; e < (size_t)dk * dv; ++e) S[e] = gL * S[e] + dS[e];
+    }
+    if (J->hT) memcpy(J->hT + ((size_t)s * H + h) * dk * dv, S, sizeof(double) * dk * dv);
+    free(S);
+    free(dS);
+}
+
+static void *worker(void *arg) {
+    job_t *J = (job_t *)arg;
+    const int total = J->units ? J->nunits : J->nseq * J->H;
+    for (;;) {
+        const int u = __atomic_fetch_add(&J->next_unit, 1, __ATOMIC_RELAXED);
+        if (u >= total) break;
+        int s, h;
+        if (J->units) { s = J->units[2 * u]; h = J->units[2 * u + 1]; }
+        else { s = u / J->H; h = u % J->H; }
+        if (s < 0 || s >= J->nseq || h < 0 || h >= J->H) { J->error = 1; continue; }
+        if (J->form == 0) chain_recurrent(J, s, h);
+        else if (J->form == 1) chain_quadratic(J, s, h);
+        else chain_chunked(J, s, h);
+    }
+    return NULL;
+}
+
+static int run(job_t *J, int nthreads) {
+    if (!J->q || !J->k || !J->v || !J->log_decay || !J->o || !J->seq_start || !J->seq_len) return -1;
+    if (J->nseq < 0 || J->H <= 0 || J->dk <= 0 || J->dv <= 0) return -1;
+    if (J->form == 2 && J->chunk <= 0) return -1;
+    for (int s = 0; s < J->nseq; ++s)
+        if (J->seq_len[s] < 0 || J->seq_start[s] < 0) return -1;
+    J->next_unit = 0;
+    J->error = 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if (nthreads == 1) {
+        worker(J);
+    } else {
+        pthread_t tid[512];
+        int started = 0;
+        for (int t = 0; t < nthreads; ++t)
+            if (pthread_create(&tid[started], NULL, worker, J) == 0) ++started;
+        if (started == 0) worker(J);
+        for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    }
+    return J->error ? -1 : 0;
+}
+
+#define JOB_INIT(FORM, CHUNK)                                                        \
+    job_t J;                                                                         \
+    memset(&J, 0, sizeof J);                                                         \
+    J.q = q; J.k = k; J.v = v; J.log_decay = log_decay; J.h0 = h0; J.o = o;          \
+    J.hT = hT; J.seq_start = seq_start; J.seq_len = seq_len; J.nseq = nseq; J.H = H; \
+    J.dk = dk; J.dv = dv; J.units = units; J.nunits = nunits; J.form = (FORM);       \
+    J.chunk = (CHUNK)
+
+int gla_oracle_recurrent(const float *q, const float *k, const float *v, const double *log_decay,
+                         const double *h0, double *o, double *hT, const int64_t *seq_start,
+                         const int64_t *seq_len, int nseq, int H, int dk, int dv,
+                         const int32_t *units, int nunits, int nthreads) {
+    JOB_INIT(0, 0);
+    return run(&J, nthreads);
+}
+
+int gla_oracle_quadratic(const float *q, const float *k, const float *v, const double *log_decay,
+                         const double *h0, double *o, double *hT, const int64_t *seq_start,
+                         const int64_t *seq_len, int nseq, int H, int dk, int dv,
+                         const int32_t *units, int nunits, int nthreads) {
+    JOB_INIT(1, 0);
+    return run(&J, nthreads);
+}
+
+int gla_oracle_chunked(const float *q, const float *k, const float *v, const double *log_decay,
+                       const double *h0, double *o, double *hT, const int64_t *seq_start,
+                       const int64_t *seq_len, int nseq, int H, int dk, int dv, int chunk,
+                       const int32_t *units, int nunits, int nthreads) {
+    JOB_INIT(2, chunk);
+    return run(&J, nthreads);
+}
+
+/*
+ * One recurrent decode step for N independent sequences, each with H heads:
+ *   state <- lambda * state + k^T v   (in place),   o = q state.
+ * [L3B] §"i14 与 Laplace 3B 架构" (GLA mixer, O(1) inference per token) and
+ * §"Trainium2 上的推理优化" (a fixed per-sequence state page read and written
+ * once per generated token).
+ *   q, k : [N, H, dk] float32;  v : [N, H, dv] float32
+ *   state: [N, H, dk, dv] float64 (in/out);  o : [N, H, dv] float64
+ */
+typedef struct {
+    const float *q, *k, *v;
+    const double *log_decay;
+    double *state, *o;
+    int N, H, dk, dv, next;
+} dec_t;
+
+static void *dec_worker(void *arg) {
+    dec_t *D = (dec_t *)arg;
+    const int H = D->H, dk = D->dk, dv = D->dv;
+    for (;;) {
+        const int u = __atomic_fetch_add(&D->next, 1, __ATOMIC_RELAXED);
+        if (u >= D->N * H) break;
+        const int h = u % H;
+        const double lam = exp(D->log_decay[h]);
+        double *S = D->state + (size_t)u * dk * dv;
+        const float *qt = D->q + (size_t)u * dk, *kt = D->k + (size_t)u * dk, *vt = D->v + (size_t)u * dv;
+        double *ot = D->o + (size_t)u * dv;
+        for (int j = 0; j < dv; ++j) ot[j] = 0.0;
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j) {
+                S[(size_t)i * dv + j] = lam * S[(size_t)i * dv + j] + (double)kt[i] * (double)vt[j];
+                ot[j] += (double)qt[i] * S[(size_t)i * dv + j];
+            }
+    }
+    return NULL;
+}
+
+int gla_oracle_decode_step(const float *q, const float *k, const float *v, const double *log_decay,
+                           double *state, double *o, int N, int H, int dk, int dv, int nthreads) {
+    if (!q || !k || !v || !log_decay || !state || !o || N < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    dec_t D = {q, k, v, log_decay, state, o, N, H, dk, dv, 0};
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    pthread_t tid[512];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&tid[started], NULL, dec_worker, &D) == 0) ++started;
+    dec_worker(&D);
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    return 0;
+}

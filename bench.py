@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the Simple GLA hot path on one GB300 (or N replicas).
+
+One step = one chunked prefill forward over the Laplace-3B-shaped layer
+(B8 T2048 H16 dk96 dv192, chunk 128, bf16) followed by one recurrent decode
+step over N1280 x H16 states (fp32 96x192), both through libgla's C ABI with
+inputs resident in HBM.  ``value`` is prefill tokens/s (tokens of the layer,
+all 16 heads, per second of prefill time, summed over replicas); the decode
+half is reported as state GB/s under ``decode``.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 the script runs under torchrun, one replica per GPU (weak scaling,
+no data-path collective); timing is the max over ranks.  ``--impl reference``
+times the fp64 CPU reference on the host instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GLA fwd tokens/s (H16,dk96,dv192,bf16) + %TC peak; decode state GB/s vs HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_bytes(B, T, H, dk, dv, with_h0, with_hT):
+    """Algorithmic HBM bytes of one prefill launch: bf16 q, k, v read, bf16 out written, f32 states."""
+    per_token_head = 2 * (dk + dk + dv + dv)
+    b = B * T * H * per_token_head
+    st = B * H * dk * dv * 4
+    return b + (st if with_h0 else 0) + (st if with_hT else 0)
+
+
+def prefill_flops(B, T, H, dk, dv, C):
+    """Tensor-core FLOPs issued per launch as full tiles: 2C(dk+dv) + 4 dk dv per token-head."""
+    return B * T * H * (2 * C * (dk + dv) + 4 * dk * dv)
+
+
+def decode_bytes(N, H, dk, dv):
+    state = N * H * dk * dv * 4 * 2
+    io = N * H * (2 * dk + 2 * dv) * 2
+    return state, io
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gla_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        finally:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, x in enumerate(r) if x.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_source, key):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[key]
+        if d.get("source_sha") == source_hash(kernel_source):
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def dist_setup(init: bool = True):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and init:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+_REF_INPUTS = {}
+
+
+def reference_inputs():
+    """The layer workload on the host (seed 0), widened once to the reference's float32 input format."""
+    if not _REF_INPUTS:
+        from gated_linear_rnn_gb300 import inputs as I
+        w = I.WORKLOADS["layer_bf16"]
+        d = I.make_prefill(w, device="cpu", seed=0)
+        _REF_INPUTS.update({k: d[k].float().numpy() for k in ("q", "k", "v")})
+        _REF_INPUTS["log_decay"] = d["log_decay"].double().numpy()
+        _REF_INPUTS["w"] = w
+    return _REF_INPUTS
+
+
+def reference_pass(row: int, threads: int) -> float:
+    """The fp64 reference over one batch row of the layer (all H heads, T tokens); returns seconds."""
+    import oracle
+    d = reference_inputs()
+    sl = slice(row, row + 1)
+    t0 = time.perf_counter()
+    oracle.recurrent(d["q"][sl], d["k"][sl], d["v"][sl], d["log_decay"], None, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_reference_rate(budget_s: float):
+    """fp64 reference (as it stands) on the host cores over rows of the layer workload, for about
+    ``budget_s`` seconds; returns (tokens/s, threads, sample description)."""
+    import oracle
+    d = reference_inputs()
+    w = d["w"]
+    threads = oracle.default_threads()
+    el, rows = 0.0, 0
+    while el < budget_s or rows == 0:
+        el += reference_pass(rows % w.B, threads)
+        rows += 1
+    sample = (f"{rows} batch row(s) of the layer workload (each: {w.H} heads x T={w.T}), "
+              f"{el:.1f} s of fp64 reference time")
+    return rows * w.T / el, threads, sample
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    d = reference_inputs()
+    w = d["w"]
+    threads = oracle.default_threads()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = reference_pass(i % w.B, threads)
+        if i >= args.warmup:
+            times.append(t)
+    tot = sum(times)
+    value = len(times) * w.T / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: the fp64 reference over one batch row ({w.H} heads x T={w.T})"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": "Laplace-3B-shaped GLA layer prefill B8 T2048 H16 dk96 dv192 chunk128 bf16 "
+                        "+ decode step N1280 x H16 (fp32 state 96x192)",
+            "global_batch": w.B, "seq_len": w.T, "heads": w.H, "dk": w.dk, "dv": w.dv, "chunk": w.chunk,
+            "decode_sequences": 1280,
+            "l2": "inputs larger than L2 every iteration (302 MB prefill io, 1.51 GB decode state); no flush"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from gated_linear_rnn_gb300 import build as Bld
+    from gated_linear_rnn_gb300 import gla
+    from gated_linear_rnn_gb300 import inputs as I
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Bld.build_library()
+    gla.load()
+    peaks, peak_src = load_peaks()
+
+    w = I.WORKLOADS["layer_bf16"]
+    wd = I.WORKLOADS["decode"]
+    P = I.make_prefill(w, device=dev, seed=rank)
+    D = I.make_decode(wd, device=dev, seed=rank)
+    B, T, H, dk, dv, C = w.B, w.T, w.H, w.dk, w.dv, w.chunk
+    out = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+    dout = torch.empty(wd.B, wd.H, wd.dv, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        gla.gla_chunk_fwd(P["q"], P["k"], P["v"], P["log_decay"], P["h0"], out, hT, C, None, stream)
+
+    def decode():
+        gla.gla_decode_step(D["q"], D["k"], D["v"], D["log_decay"], D["state"], dout, stream)
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    if gla.gla_last_device_status(stream) != 0:
+        raise SystemExit("device status after warm-up is not ok")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches0 = gla.gla_kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    launches = gla.gla_kernel_launches() - launches0
+    pre_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    pre_total = max_over_ranks(sum(pre_ms), world)
+    dec_total = max_over_ranks(sum(dec_ms), world)
+    step_total = max_over_ranks(sum(step_ms), world)
+    if gla.gla_last_device_status(stream) != 0:
+        raise SystemExit("device status after the timed region is not ok")
+
+    tokens = B * T * args.steps * world
+    value = tokens / (pre_total / 1e3)
+    pbytes = prefill_bytes(B, T, H, dk, dv, P["h0"] is not None, True)
+    pflops = prefill_flops(B, T, H, dk, dv, C)
+    pre_avg_s = pre_total / args.steps / 1e3
+    achieved_gbs = pbytes / pre_avg_s / 1e9
+    tc_tflops = pflops / pre_avg_s / 1e12
+    tc_kernel = os.path.join(ROOT, "gated_linear_rnn_gb300", "csrc", "gla_tc.cu")
+    sbytes, iobytes = decode_bytes(wd.B, wd.H, wd.dk, wd.dv)
+    dec_avg_s = dec_total / args.steps / 1e3
+
+    # ---- end to end through the public API: pinned host inputs in, results back to the host ----
+    e2e = run_e2e(args, P, D, w, wd, out, hT, dout, stream)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w),
+        "prefill_ms": pre_total / args.steps, "decode_ms": dec_total / args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": recorded_traffic(tc_kernel, "prefill_layer_bf16"),
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "kernel": "gla_chunk_fwd (layer_bf16)",
+                     "algorithmic_bytes_per_launch": pbytes,
+                     "tensor": {"achieved_tflops": tc_tflops, "peak_tflops": peaks["bf16_tflops"],
+                                "frac": tc_tflops / peaks["bf16_tflops"],
+                                "flops_per_launch": pflops, "peak_source": f"{peak_src} bf16 dense (burst)"}},
+        "decode": {"value": sbytes / dec_avg_s / 1e9, "unit": "state GB/s",
+                   "total_gbs": (sbytes + iobytes) / dec_avg_s / 1e9,
+                   "frac_of_hbm_peak": (sbytes + iobytes) / dec_avg_s / 1e9 / peaks["hbm_gbs"],
+                   "us_per_step": dec_avg_s * 1e6, "state_bytes": sbytes, "io_bytes": iobytes,
+                   "tokens_per_s": wd.B * world / dec_avg_s},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, sample = cpu_reference_rate(args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(args, P, D, w, wd, out, hT, dout, stream):
+    """Same step through the public API with host buffers: H2D of inputs, compute, D2H of results."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    host = {k: P[k].cpu().pin_memory() for k in ("q", "k", "v")}
+    hostd = {k: D[k].cpu().pin_memory() for k in ("q", "k", "v")}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_hT = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    h_dout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    dq, dk_, dv_ = (torch.empty_like(P[k]) for k in ("q", "k", "v"))
+    eq, ek, evv = (torch.empty_like(D[k]) for k in ("q", "k", "v"))
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(hostd.values()))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_hT, h_dout))
+    steps = max(1, min(args.steps, 10))
+
+    def prefill_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dk_.copy_(host["k"], non_blocking=True)
+        dv_.copy_(host["v"], non_blocking=True)
+        gla.gla_chunk_fwd(dq, dk_, dv_, P["log_decay"], P["h0"], out, hT, w.chunk, None, stream)
+        h_out.copy_(out, non_blocking=True)
+        h_hT.copy_(hT, non_blocking=True)
+
+    def decode_step():
+        eq.copy_(hostd["q"], non_blocking=True)
+        ek.copy_(hostd["k"], non_blocking=True)
+        evv.copy_(hostd["v"], non_blocking=True)
+        gla.gla_decode_step(eq, ek, evv, D["log_decay"], D["state"], dout, stream)
+        h_dout.copy_(dout, non_blocking=True)
+
+    prefill_step()
+    decode_step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        evs[i][0].record(stream)
+        prefill_step()
+        evs[i][1].record(stream)
+        decode_step()
+        evs[i][2].record(stream)
+    torch.cuda.synchronize()
+    pre_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    sbytes, _ = decode_bytes(wd.B, wd.H, wd.dk, wd.dv)
+    return {"value": w.B * w.T / (pre_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "prefill_ms": pre_ms, "decode_ms": dec_ms, "steps": steps,
+            "decode_state_gbs": sbytes / (dec_ms / 1e3) / 1e9,
+            "note": "pinned host q,k,v copied in and out/hT/decode-out copied back every step; "
+                    "the decode state stays resident on the device"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of fp64 reference work to time")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # the CPU reference arm: rank 0 alone works, no process group is needed
+        world, rank, _ = dist_setup(init=False)
+        return run_reference(args, world, rank)
+    world, rank, local = dist_setup()
+    try:
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+// gla_capi.cu — the extern "C" boundary of libgla.so.
+//
+// Host-side argument checks, the choice between the tensor-core and SIMT
+// kernels, and the device status word.  Declarations and the contract of every
+// entry point are in include/gla.h.
+#include <atomic>
+#include <mutex>
+
+#include "gla_common.cuh"
+
+namespace gla {
+
+// kernels (defined in the other translation units)
+int simt_chunk_fwd_f32(const float *, const float *, const float *, const float *, const float *, float *,
+                       float *, int, int, int, int, int, int, const int32_t *, cudaStream_t);
+int simt_chunk_fwd_bf16(const void *, const void *, const void *, const float *, const float *, void *,
+                        float *, int, int, int, int, int, int, const int32_t *, cudaStream_t);
+int decode_step_bf16(const void *, const void *, const void *, const float *, float *, void *, int, int, int,
+                     int, cudaStream_t);
+int decode_step_f32(const float *, const float *, const float *, const float *, float *, float *, int, int,
+                    int, int, cudaStream_t);
+bool tc_chunk_supported(int dk, int dv, int chunk);
+int tc_chunk_fwd_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *,
+                      int, int, int, int, int, const int32_t *, cudaStream_t);
+int take_status_simt(cudaStream_t);
+int take_status_decode(cudaStream_t);
+int take_status_tc(cudaStream_t);
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+constexpr int kMaxDevices = 64;
+std::once_flag g_once[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+const DeviceInfo &device_info() {
+    static DeviceInfo none = {0, 0, 0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return none;
+    std::call_once(g_once[dev], [dev]() {
+        DeviceInfo d = {0, 0, 0};
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        d.ok = (major == 10 && minor == 3) ? 1 : 0;
+        g_info[dev] = d;
+    });
+    return g_info[dev];
+}
+
+namespace {
+
+int check_decays_and_sizes(const float *log_decay, int B, int T, int H, int dk, int dv) {
+    if (log_decay == nullptr) return GLA_ERR_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || dk <= 0 || dv <= 0) return GLA_ERR_ARG;
+    return GLA_OK;
+}
+
+int check_prefill(const void *q, const void *k, const void *v, const float *ld, const float *h0, const void *out,
+                  const float *hT, int B, int T, int H, int dk, int dv, const int32_t *cu) {
+    if (!q || !k || !v || !out) return GLA_ERR_ARG;
+    int rc = check_decays_and_sizes(ld, B, T, H, dk, dv);
+    if (rc) return rc;
+    if (dk < 16 || dk > 256 || dv < 16 || dv > 512 || dk % 8 || dv % 8) return GLA_ERR_UNSUPPORTED;
+    if ((long long)B * T * H > (1LL << 40)) return GLA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(h0) ||
+        !aligned16(hT) || !aligned16(ld) || !aligned16(cu))
+        return GLA_ERR_ALIGN;
+    if (!device_info().ok) return GLA_ERR_UNSUPPORTED;
+    return GLA_OK;
+}
+
+int check_decode(const void *q, const void *k, const void *v, const float *ld, const float *state,
+                 const void *out, int N, int H, int dk, int dv) {
+    if (!q || !k || !v || !out || !state) return GLA_ERR_ARG;
+    int rc = check_decays_and_sizes(ld, N, 1, H, dk, dv);
+    if (rc) return rc;
+    if (dk > 256 || dv < 4 || dv > 1024 || dv % 4) return GLA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(state) ||
+        !aligned16(ld))
+        return GLA_ERR_ALIGN;
+    if (!device_info().ok) return GLA_ERR_UNSUPPORTED;
+    return GLA_OK;
+}
+
+}  // namespace
+}  // namespace gla
+
+using namespace gla;
+
+extern "C" {
+
+int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_decay, const float *h0,
+                  void *out, float *hT, int B, int T, int H, int dk, int dv, int chunk,
+                  const int32_t *cu_seqlens, void *stream) {
+    int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+        return tc_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens, st);
+    return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
+}
+
+int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *log_decay, const float *h0,
+                      float *out, float *hT, int B, int T, int H, int dk, int dv, int chunk,
+                      const int32_t *cu_seqlens, void *stream) {
+    int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    return simt_chunk_fwd_f32(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens,
+                              (cudaStream_t)stream);
+}
+
+int gla_decode_step(const void *q, const void *k, const void *v, const float *log_decay, float *state_inout,
+                    void *out, int N, int H, int dk, int dv, void *stream) {
+    int rc = check_decode(q, k, v, log_decay, state_inout, out, N, H, dk, dv);
+    if (rc) return rc;
+    return decode_step_bf16(q, k, v, log_decay, state_inout, out, N, H, dk, dv, (cudaStream_t)stream);
+}
+
+int gla_decode_step_f32(const float *q, const float *k, const float *v, const float *log_decay,
+                        float *state_inout, float *out, int N, int H, int dk, int dv, void *stream) {
+    int rc = check_decode(q, k, v, log_decay, state_inout, out, N, H, dk, dv);
+    if (rc) return rc;
+    return decode_step_f32(q, k, v, log_decay, state_inout, out, N, H, dk, dv, (cudaStream_t)stream);
+}
+
+int gla_last_device_status(void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    int result = GLA_OK;
+    const int parts[3] = {take_status_simt(st), take_status_decode(st), take_status_tc(st)};
+    for (int p : parts) {
+        if (p == GLA_ERR_LAUNCH) return GLA_ERR_LAUNCH;
+        if (result == GLA_OK && p != 0) result = p;
+    }
+    return result;
+}
+
+const char *gla_status_str(int status) {
+    switch (status) {
+        case GLA_OK: return "ok";
+        case GLA_ERR_ARG: return "invalid argument";
+        case GLA_ERR_UNSUPPORTED: return "unsupported shape, chunk or device";
+        case GLA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case GLA_ERR_LAUNCH: return "CUDA call or kernel launch failed";
+        case GLA_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case GLA_ERR_NOMEM: return "scratch allocation failed";
+        case GLA_ERR_DEVICE_ARG: return "invalid cu_seqlens found on the device";
+        default: return "unknown status";
+    }
+}
+
+uint64_t gla_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int gla_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,215 @@
+"""Thin Python binding of libgla.so (argument marshalling only).
+
+The functions named ``gla_*`` mirror the C entry points of include/gla.h one to
+one: they take torch tensors that already live on the current CUDA device,
+check dtype / shape / contiguity, pass raw pointers and the current stream, and
+raise ``GLAError`` on a non-zero status.  ``chunk_fwd`` and ``decode_step`` are
+conveniences that allocate the outputs with torch and call those entry points.
+Every step of the computation runs in the library's CUDA kernels; when the
+library is missing this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgla.so")
+
+STATUS = {0: "GLA_OK", -1: "GLA_ERR_ARG", -2: "GLA_ERR_UNSUPPORTED", -3: "GLA_ERR_ALIGN", -4: "GLA_ERR_LAUNCH",
+          -5: "GLA_ERR_TIMEOUT", -6: "GLA_ERR_NOMEM", -7: "GLA_ERR_DEVICE_ARG"}
+
+# C signatures (argtypes, restype) of every exported entry point, as declared in include/gla.h
+_P, _I = ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "gla_chunk_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_decode_step": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "gla_decode_step_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "gla_last_device_status": ([_P], _I),
+    "gla_status_str": ([_I], ctypes.c_char_p),
+    "gla_kernel_launches": ([], ctypes.c_uint64),
+    "gla_version": ([], _I),
+}
+
+
+class GLAError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_status_text(status)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libgla.so once (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build it with gated_linear_rnn_gb300.build.build_library()")
+            lib = ctypes.CDLL(p)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load().gla_status_str(int(status)).decode()
+    except Exception:  # library not loadable: plain name only
+        return STATUS.get(status, "unknown")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(t: Optional[torch.Tensor], name: str, dtype, shape=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _raise(rc: int, what: str):
+    if rc != 0:
+        raise GLAError(rc, what)
+
+
+# ---- entry points (same names as the C ABI) ---------------------------------------------------
+
+def _chunk_args(q, k, v, log_decay, h0, out, hT, cu_seqlens, dtype):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, dk] (packed: [1, T, H, dk])")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q", dtype)
+    _check(k, "k", dtype, (B, T, H, dk))
+    _check(v, "v", dtype, (B, T, H, dv))
+    _check(out, "out", dtype, (B, T, H, dv))
+    _check(log_decay, "log_decay", torch.float32, (H,))
+    nseq = B
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("a packed batch has leading dimension 1")
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+        nseq = cu_seqlens.numel() - 1
+    _check(h0, "h0", torch.float32, (nseq, H, dk, dv), allow_none=True)
+    _check(hT, "hT", torch.float32, (nseq, H, dk, dv), allow_none=True)
+    return nseq, T, H, dk, dv
+
+
+def gla_chunk_fwd(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, stream=None) -> None:
+    """bf16 chunked forward: writes ``out`` and (if given) ``hT``.  See include/gla.h."""
+    nseq, T, H, dk, dv = _chunk_args(q, k, v, log_decay, h0, out, hT, cu_seqlens, torch.bfloat16)
+    rc = load().gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
+                              nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_chunk_fwd")
+
+
+def gla_chunk_fwd_f32(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, stream=None) -> None:
+    """f32 chunked forward (SIMT kernel).  See include/gla.h."""
+    nseq, T, H, dk, dv = _chunk_args(q, k, v, log_decay, h0, out, hT, cu_seqlens, torch.float32)
+    rc = load().gla_chunk_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
+                                  nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_chunk_fwd_f32")
+
+
+def _decode_args(q, k, v, log_decay, state, out, dtype):
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, dk]")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q", dtype)
+    _check(k, "k", dtype, (N, H, dk))
+    _check(v, "v", dtype, (N, H, dv))
+    _check(out, "out", dtype, (N, H, dv))
+    _check(log_decay, "log_decay", torch.float32, (H,))
+    _check(state, "state_inout", torch.float32, (N, H, dk, dv))
+    return N, H, dk, dv
+
+
+def gla_decode_step(q, k, v, log_decay, state_inout, out, stream=None) -> None:
+    """bf16 decode step: updates ``state_inout`` in place and writes ``out``."""
+    N, H, dk, dv = _decode_args(q, k, v, log_decay, state_inout, out, torch.bfloat16)
+    rc = load().gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(state_inout), _ptr(out),
+                                N, H, dk, dv, _stream(stream))
+    _raise(rc, "gla_decode_step")
+
+
+def gla_decode_step_f32(q, k, v, log_decay, state_inout, out, stream=None) -> None:
+    N, H, dk, dv = _decode_args(q, k, v, log_decay, state_inout, out, torch.float32)
+    rc = load().gla_decode_step_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(state_inout), _ptr(out),
+                                    N, H, dk, dv, _stream(stream))
+    _raise(rc, "gla_decode_step_f32")
+
+
+def gla_last_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the library's device status word."""
+    return int(load().gla_last_device_status(_stream(stream)))
+
+
+def gla_status_str(status: int) -> str:
+    return load().gla_status_str(int(status)).decode()
+
+
+def gla_kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load().gla_kernel_launches())
+
+
+def gla_version() -> int:
+    return int(load().gla_version())
+
+
+# ---- conveniences ---------------------------------------------------------------------------
+
+def chunk_fwd(q, k, v, log_decay, h0=None, chunk: int = 128, cu_seqlens=None, final_state: bool = True,
+              stream=None):
+    """Allocate ``out`` (and ``hT``) and run the chunked forward; returns (out, hT or None)."""
+    nseq = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+    out = torch.empty(q.shape[:3] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    hT = torch.empty((nseq, q.shape[2], q.shape[3], v.shape[-1]), dtype=torch.float32, device=q.device) \
+        if final_state else None
+    if q.dtype == torch.float32:
+        gla_chunk_fwd_f32(q, k, v, log_decay, h0, out, hT, chunk, cu_seqlens, stream)
+    else:
+        gla_chunk_fwd(q, k, v, log_decay, h0, out, hT, chunk, cu_seqlens, stream)
+    return out, hT
+
+
+def decode_step(q, k, v, log_decay, state, stream=None):
+    """Run one decode step in place on ``state``; returns the new ``out`` tensor."""
+    out = torch.empty(q.shape[:2] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    if q.dtype == torch.float32:
+        gla_decode_step_f32(q, k, v, log_decay, state, out, stream)
+    else:
+        gla_decode_step(q, k, v, log_decay, state, out, stream)
+    return out

@@ -1,0 +1,161 @@
+/*
+ * gla.h — C ABI of libgla.so: Simple Gated Linear Attention (Simple GLA) on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (page "线性注意力模型如何实现固定推理状态" — Beyond the KV cache:
+ * training and serving i14's Laplace 3B linear attention model on AWS
+ * Trainium2 — section "i14 与 Laplace 3B 架构", GLA mixer and decay scheme):
+ * every head h keeps a dk x dv matrix state S and a fixed, non-learned scalar
+ * decay lambda_h = exp(log_decay[h]) in (0, 1].  For each token t
+ *
+ *     S_t = lambda_h * S_{t-1} + k_t^T v_t          (state update)
+ *     o_t = q_t S_t                                 (read-out, after the update)
+ *
+ * with k_t, q_t in R^{1 x dk}, v_t, o_t in R^{1 x dv}.  There is no extra
+ * scale: any 1/sqrt(dk) belongs to the caller's q.
+ *
+ * Conventions shared by every entry point
+ *   - Layouts are row-major with the innermost dimension last.
+ *   - Every pointer argument is a DEVICE pointer of the current CUDA device and
+ *     must be 16-byte aligned (GLA_ERR_ALIGN otherwise).  The caller owns every
+ *     buffer; the library never frees or keeps a caller pointer.
+ *   - "bf16" means IEEE-754 binary16-bfloat (torch.bfloat16); "f32" float.
+ *     States (h0, hT, state_inout) and log_decay are always f32, and all
+ *     accumulation is f32.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: the return value covers host-side argument checks and the
+ *     launch.  Failures found on the device (a bounded wait that ran out, a bad
+ *     cu_seqlens entry) are recorded in a device status word that
+ *     gla_last_device_status() returns and clears.
+ *   - Inputs and outputs must not overlap, except state_inout, which is
+ *     updated in place.
+ *   - Thread-safe: the only global state is a per-device capability cache and
+ *     the device status word.
+ *   - The library needs an sm_103a device (GB300); on any other device every
+ *     compute entry point returns GLA_ERR_UNSUPPORTED.
+ */
+#ifndef GLA_H_
+#define GLA_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GLA_API __attribute__((visibility("default")))
+#else
+#define GLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GLA_OK = 0,
+    GLA_ERR_ARG = -1,          /* null pointer, non-positive size, inconsistent sizes */
+    GLA_ERR_UNSUPPORTED = -2,  /* shape / chunk outside what the kernels handle, or not sm_103a */
+    GLA_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned */
+    GLA_ERR_LAUNCH = -4,       /* a CUDA call or kernel launch failed */
+    GLA_ERR_TIMEOUT = -5,      /* device: a bounded pipeline wait gave up (reported by gla_last_device_status) */
+    GLA_ERR_NOMEM = -6,        /* stream-ordered scratch allocation failed */
+    GLA_ERR_DEVICE_ARG = -7    /* device: cu_seqlens not non-decreasing / out of [0, T] (gla_last_device_status) */
+} gla_status;
+
+/*
+ * gla_chunk_fwd — chunkwise-parallel prefill / training forward, bf16 q, k, v, out.
+ *
+ * Computes, for every sequence and head, the recurrence above over all tokens
+ * in chunks of `chunk` tokens (page "线性注意力模型如何实现固定推理状态",
+ * section "挑战 1", chunked GLA and Figure 3): within chunk c of length L
+ * (local positions i, j)
+ *     O_c = ((Q_c K_c^T) .* D) V_c + diag(lambda^(i+1)) Q_c S_{c-1},
+ *           D_ij = lambda^(i-j) if j <= i else 0,
+ *     S_c = lambda^L S_{c-1} + K_c^T diag(lambda^(L-1-j)) V_c,
+ * which equals the token-by-token recurrence up to rounding.
+ *
+ * Arguments
+ *   q, k       [B, T, H, dk] bf16           (packed: [1, T, H, dk])
+ *   v          [B, T, H, dv] bf16           (packed: [1, T, H, dv])
+ *   log_decay  [H] f32, natural log of lambda_h, each <= 0 and finite
+ *   h0         [B, H, dk, dv] f32 initial state, or NULL for zeros
+ *   out        [B, T, H, dv] bf16, written
+ *   hT         [B, H, dk, dv] f32 final state, written; or NULL to skip
+ *   B, T, H    batch, tokens per sequence, heads (all > 0)
+ *   dk, dv     key / value head sizes: 16 <= dk <= 256 and 16 <= dv <= 512,
+ *              both multiples of 8
+ *   chunk      chunk length: 128 selects the tensor-core kernel (tcgen05/TMEM,
+ *              fed by TMA) when 32 | dk <= 128 and 64 | dv <= 192; 16, 32 or 64
+ *              (and 128 outside that envelope) run the SIMT kernel, which
+ *              splits a chunk that does not fit in shared memory in halves
+ *   cu_seqlens NULL for a dense batch.  Otherwise a DEVICE int32 array [B+1]
+ *              of packed sequence offsets: sequence s is rows
+ *              cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed [1, T, ...]
+ *              tensors, B is the number of sequences, T the total rows, and
+ *              h0 / hT are [B, H, dk, dv].  Chunks restart at every sequence
+ *              start; an empty sequence gets hT = h0.  Offsets must be
+ *              non-decreasing within [0, T]; a sequence that violates this is
+ *              skipped and GLA_ERR_DEVICE_ARG is recorded on the device.
+ *   stream     cudaStream_t
+ * Long dense sequences with few (sequence, head) chains may be split into
+ * segments whose boundary states are found in a first pass; that schedule
+ * takes stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`,
+ * GLA_ERR_NOMEM on failure).  Returns a gla_status.
+ */
+GLA_API int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_decay,
+                  const float *h0, void *out, float *hT, int B, int T, int H, int dk, int dv,
+                  int chunk, const int32_t *cu_seqlens, void *stream);
+
+/* gla_chunk_fwd_f32 — as gla_chunk_fwd with f32 q, k, v and out.  Always runs
+ * the SIMT kernel (f32 FMA, no tensor cores): chunk in {16, 32, 64, 128}.
+ * The SIMT kernel processes a chunk whose tiles do not fit in shared memory
+ * (large dk) as sub-chunks of half the length; the result is the same map. */
+GLA_API int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *log_decay,
+                      const float *h0, float *out, float *hT, int B, int T, int H, int dk, int dv,
+                      int chunk, const int32_t *cu_seqlens, void *stream);
+
+/*
+ * gla_decode_step — one recurrent decode step for N independent sequences
+ * (page "线性注意力模型如何实现固定推理状态", section "i14 与 Laplace 3B 架构":
+ * O(1) work per generated token with a fixed-size state; section "Trainium2 上的
+ * 推理优化": one fixed state page per sequence):
+ *     state <- lambda_h * state + k^T v      (in place)
+ *     out    = q state                        (with the updated state)
+ *
+ *   q, k         [N, H, dk] bf16
+ *   v            [N, H, dv] bf16
+ *   log_decay    [H] f32
+ *   state_inout  [N, H, dk, dv] f32, read and written once
+ *   out          [N, H, dv] bf16, written
+ *   N, H > 0; 1 <= dk <= 256; 4 <= dv <= 1024 with dv % 4 == 0
+ *   stream       cudaStream_t
+ * Returns a gla_status.
+ */
+GLA_API int gla_decode_step(const void *q, const void *k, const void *v, const float *log_decay,
+                    float *state_inout, void *out, int N, int H, int dk, int dv, void *stream);
+
+/* gla_decode_step_f32 — as gla_decode_step with f32 q, k, v and out. */
+GLA_API int gla_decode_step_f32(const float *q, const float *k, const float *v, const float *log_decay,
+                        float *state_inout, float *out, int N, int H, int dk, int dv, void *stream);
+
+/*
+ * gla_last_device_status — synchronise `stream`, then return and clear the
+ * device status word: GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_DEVICE_ARG for the
+ * first failure recorded by any kernel of this library on the current device
+ * since the previous call.  Returns GLA_ERR_LAUNCH if synchronisation fails.
+ */
+GLA_API int gla_last_device_status(void *stream);
+
+/* gla_status_str — static, NUL-terminated description of a gla_status value. */
+GLA_API const char *gla_status_str(int status);
+
+/* gla_kernel_launches — number of CUDA kernels this library has launched in
+ * this process (all devices, all threads), counted on the host at launch. */
+GLA_API uint64_t gla_kernel_launches(void);
+
+/* gla_version — library version as major*10000 + minor*100 + patch. */
+GLA_API int gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLA_H_ */

@@ -1,0 +1,213 @@
+"""GPU parity: every CUDA path against the fp64 reference, through the C ABI.
+
+Bar (per tensor, O and the final state separately): max|gpu - ref| / max|ref|
+<= 1e-2 for bf16 inputs (f32 accumulate) and <= 1e-4 for f32 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_linear_rnn_gb300 import build as B
+from gated_linear_rnn_gb300 import gla
+from gated_linear_rnn_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "f32": 1e-4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    B.build_library()
+    gla.load()
+    torch.cuda.set_device(0)
+    yield
+    assert gla.gla_last_device_status() == 0
+
+
+def run_prefill(d, chunk):
+    out, hT = gla.chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], chunk=chunk,
+                            cu_seqlens=d["cu_dev"])
+    torch.cuda.synchronize()
+    return out, hT
+
+
+def with_dev_cu(d):
+    d["cu_dev"] = None if d["cu_seqlens"] is None else d["cu_seqlens"].cuda()
+    return d
+
+
+def check_prefill(w, chunk=None, units=None, seed=0, **kw):
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=seed, **kw))
+    chunk = chunk or w.chunk
+    out, hT = run_prefill(d, chunk)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"],
+                                    cu_seqlens=d["cu_seqlens"], units=units)
+    o = out.float().cpu().numpy()
+    h = hT.cpu().numpy()
+    if units is not None:
+        # compare only the sampled chains
+        sel_o, sel_r, sel_h, sel_hr = [], [], [], []
+        cu = d["cu_seqlens"]
+        for s, hh in units:
+            if cu is None:
+                sel_o.append(o[s, :, hh]); sel_r.append(o_ref[s, :, hh])
+            else:
+                a, b = int(cu[s]), int(cu[s + 1])
+                sel_o.append(o[0, a:b, hh]); sel_r.append(o_ref[0, a:b, hh])
+            sel_h.append(h[s, hh]); sel_hr.append(h_ref[s, hh])
+        o, o_ref = np.concatenate(sel_o), np.concatenate(sel_r)
+        h, h_ref = np.stack(sel_h), np.stack(sel_hr)
+    eo, eh = oracle.rel_err(o, o_ref), oracle.rel_err(h, h_ref)
+    tol = TOL[w.dtype]
+    assert eo <= tol and eh <= tol, f"out {eo:.3e} hT {eh:.3e} (tol {tol})"
+    assert np.isfinite(o).all() and np.isfinite(h).all()
+    return eo, eh
+
+
+# ---- the small fp32 workload, whole ----
+def test_tiny_f32_workload():
+    check_prefill(I.WORKLOADS["tiny_f32"])
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128])
+def test_f32_chunks_ragged_tail(chunk):
+    w = I.scaled(I.WORKLOADS["tiny_f32"], B=2, T=200, H=3, h0_std=0.5)
+    check_prefill(w, chunk=chunk, seed=1)
+
+
+# ---- bf16: several chunks and a ragged tail, every chunk size ----
+@pytest.mark.parametrize("chunk", [16, 32, 64, 128])
+def test_bf16_layer_shapes_small(chunk):
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=300, H=4, h0_std=0.02)
+    check_prefill(w, chunk=chunk, seed=2)
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 64), (64, 64), (64, 128), (128, 192), (96, 128), (128, 64),
+                                   (48, 80), (16, 16), (256, 64)])
+def test_bf16_other_head_sizes(dk, dv):
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=260, H=2, dk=dk, dv=dv, h0_std=0.1)
+    check_prefill(w, chunk=128, seed=3)
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 256, 385])
+def test_bf16_lengths(T):
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=T, H=2, h0_std=0.05)
+    check_prefill(w, chunk=128, seed=4)
+
+
+def test_ragged_small_with_empty_and_unit_sequences():
+    w = I.scaled(I.WORKLOADS["ragged"], H=3)
+    lengths = [0, 1, 127, 128, 129, 300, 5, 0, 257]
+    check_prefill(w, lengths=lengths, seed=5)
+
+
+def test_decay_extremes():
+    """lambda = 1 (log_decay 0) and a vanishing decay in the same launch."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=300, H=2, h0_std=0.0)
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=6))
+    d["log_decay"] = torch.tensor([0.0, -30.0], device="cuda")
+    out, hT = run_prefill(d, 128)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], None)
+    assert oracle.rel_err(out.float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
+
+
+# ---- invariants on the GPU path ----
+def test_deterministic_and_causal():
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=400, H=4, h0_std=0.02)
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=7))
+    o1, h1 = run_prefill(d, 128)
+    o2, h2 = run_prefill(d, 128)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    d["q"][:, -1] += 1
+    d["k"][:, -1] -= 1
+    d["v"][:, -1] *= -1
+    o3, _ = run_prefill(d, 128)
+    assert torch.equal(o1[:, :-1], o3[:, :-1])
+
+
+def test_resume_from_final_state():
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=512, H=2, h0_std=0.02)
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=8))
+    o, hT = run_prefill(d, 128)
+    T1 = 256
+    oa, ha = gla.chunk_fwd(d["q"][:, :T1].contiguous(), d["k"][:, :T1].contiguous(), d["v"][:, :T1].contiguous(),
+                           d["log_decay"], d["h0"], chunk=128)
+    ob, hb = gla.chunk_fwd(d["q"][:, T1:].contiguous(), d["k"][:, T1:].contiguous(), d["v"][:, T1:].contiguous(),
+                           d["log_decay"], ha, chunk=128)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(torch.cat([oa, ob], 1).float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hb.cpu().numpy(), h_ref) <= 1e-2
+
+
+def test_single_token_prefill_equals_decode_step():
+    w = I.scaled(I.WORKLOADS["decode"], B=6)
+    d = I.make_decode(w, device="cuda", seed=9)
+    s = d["state"].clone()
+    o_dec = gla.decode_step(d["q"], d["k"], d["v"], d["log_decay"], s)
+    o_pre, h_pre = gla.chunk_fwd(d["q"][:, None].contiguous(), d["k"][:, None].contiguous(),
+                                 d["v"][:, None].contiguous(), d["log_decay"], d["state"], chunk=128)
+    torch.cuda.synchronize()
+    assert oracle.rel_err(o_pre[:, 0].float().cpu().numpy(), o_dec.float().cpu().numpy()) <= 1e-2
+    assert oracle.rel_err(h_pre.cpu().numpy(), s.cpu().numpy()) <= 1e-2
+
+
+# ---- decode ----
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk,dv", [(96, 192), (64, 64), (100, 36), (8, 1024)])
+def test_decode_step(dtype, dk, dv):
+    w = I.scaled(I.WORKLOADS["decode"], B=37, H=3, dk=dk, dv=dv, dtype=dtype)
+    d = I.make_decode(w, device="cuda", seed=10)
+    s0 = d["state"].clone()
+    o = gla.decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["state"])
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle.decode_step(d["q"], d["k"], d["v"], d["log_decay"], s0)
+    tol = TOL[dtype]
+    assert oracle.rel_err(o.float().cpu().numpy(), o_ref) <= tol
+    assert oracle.rel_err(d["state"].cpu().numpy(), s_ref) <= tol
+
+
+def test_decode_workload_full_size():
+    """N = 1280 sequences x 16 heads, the launch the benchmark times."""
+    w = I.WORKLOADS["decode"]
+    d = I.make_decode(w, device="cuda", seed=0)
+    s0 = d["state"].clone()
+    o = gla.decode_step(d["q"], d["k"], d["v"], d["log_decay"], d["state"])
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle.decode_step(d["q"], d["k"], d["v"], d["log_decay"], s0)
+    assert oracle.rel_err(o.float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(d["state"].cpu().numpy(), s_ref) <= 1e-2
+
+
+# ---- full-size workloads, sampled chains ----
+def test_layer_workload_full_size():
+    w = I.WORKLOADS["layer_bf16"]
+    units = [(b, h) for b in range(8) for h in range(16)]
+    check_prefill(w, units=units)
+
+
+def test_long_workload_full_size_sampled():
+    w = I.WORKLOADS["long_bf16"]
+    check_prefill(w, units=[(0, 0), (0, 5), (0, 15)])
+
+
+def test_ragged_workload_full_size_sampled():
+    w = I.WORKLOADS["ragged"]
+    lengths = I.ragged_lengths(w.ragged_n, w.ragged_max, 0)
+    order = torch.argsort(lengths)
+    units = [(int(order[0]), 0), (int(order[-1]), 15), (int(order[31]), 7), (3, 3)]
+    check_prefill(w, units=units)
+
+
+# ---- errors recorded on the device ----
+def test_bad_cu_seqlens_is_reported_not_trapped():
+    w = I.scaled(I.WORKLOADS["ragged"], H=2)
+    d = I.make_prefill(w, device="cuda", lengths=[10, 20, 30])
+    bad = torch.tensor([0, 25, 20, 60], dtype=torch.int32, device="cuda")  # decreasing offsets
+    out = torch.zeros_like(d["v"])
+    gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, None, 128, bad)
+    assert gla.gla_last_device_status() == -7
+    assert gla.gla_last_device_status() == 0  # cleared

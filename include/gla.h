@@ -83,7 +83,8 @@ typedef enum {
  *   dk, dv     key / value head sizes: 16 <= dk <= 256 and 16 <= dv <= 512,
  *              both multiples of 8
  *   chunk      chunk length: 128 selects the tensor-core kernel (tcgen05/TMEM,
- *              fed by TMA) when 32 | dk <= 128 and 64 | dv <= 192; 16, 32 or 64
+ *              fed by TMA) when 32 | dk <= 128 and 64 | dv <= 192 and its tiles fit
+ *              in shared memory (every such shape but dk = 128 with dv = 192); 16, 32 or 64
  *              (and 128 outside that envelope) run the SIMT kernel, which
  *              splits a chunk that does not fit in shared memory in halves
  *   cu_seqlens NULL for a dense batch.  Otherwise a DEVICE int32 array [B+1]

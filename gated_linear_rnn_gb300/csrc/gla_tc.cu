@@ -20,12 +20,17 @@
 // accumulator are never read.
 //
 // Warp roles (320 threads):
-//   warps 0-7  "compute": two warpgroups; thread t owns TMEM lane t % 128 (a
-//              token row of A/P/O, a dk row of S) and half of the columns.
+//   warps 0-3  "state" warpgroup: thread t owns TMEM lane t (a dk row of S).
 //              Per chunk: state pass (read S_{c-1} from TMEM, write its bf16
-//              copy for MMA3, pre-scale it by lambda^L for MMA4), decay of Q
-//              and K rows in place, decay mask A -> P, output epilogue.
-//   warp 8     TMA producer: Q (single buffer), K and V (double buffer).
+//              copy for MMA3, pre-scale it by lambda^L for MMA4), then the
+//              decays of the Q and K rows in place (after MMA1 read them).
+//   warps 4-7  "output" warpgroup: thread t owns TMEM lane t - 128 (a token
+//              row).  Per chunk: decay mask A -> P, then the output epilogue:
+//              O (TMEM) -> bf16 into the chunk's V tile (free once MMA2 and
+//              MMA4 are done) -> TMA store, which is also what releases the
+//              chunk's K/V stage to the producer.
+//   warp 8     TMA producer: Q (single buffer), K and V (double buffer), plus
+//              an L2 prefetch of the next chunk.
 //   warp 9     MMA issuer and TMEM owner.
 // Hand-offs are mbarriers; every wait is bounded (see sm100_ptx.cuh) and a
 // timeout is recorded as GLA_ERR_TIMEOUT in the device status word.
@@ -52,7 +57,6 @@ using namespace ptx;
 
 constexpr int kC = 128;              // chunk length (MMA M and the token K extent)
 constexpr int kThreads = 320;        // 8 compute warps + producer + MMA warp
-constexpr int kComputeThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -103,33 +107,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void scale_row_bf16(uint8_t *row, int nbytes, float f) {
-    // nbytes is a multiple of 16; rows keep their 16-byte chunks whatever the swizzle
-    for (int b = 0; b < nbytes; b += 16) {
-        uint4 x = *reinterpret_cast<uint4 *>(row + b);
-        uint32_t w[4] = {x.x, x.y, x.z, x.w};
+// Multiply the 16-byte chunk at `p` (8 bf16) by f, in place.
+__device__ __forceinline__ void scale_chunk_bf16(uint8_t *p, float f) {
+    uint4 x = *reinterpret_cast<uint4 *>(p);
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&w[e]);
-            float2 fl = __bfloat1622float2(h);
-            w[e] = pack_bf16x2(fl.x * f, fl.y * f);
-        }
-        *reinterpret_cast<uint4 *>(row + b) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int e = 0; e < 4; ++e) {
+        const float2 fl = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[e]));
+        w[e] = pack_bf16x2(fl.x * f, fl.y * f);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Scale row r of a [128 x dk] tile stored as 64B-swizzled atoms (8 KB each).  The
+// swizzle only permutes the four 16-byte chunks inside a row, and every chunk gets
+// the same factor, so the row is walked in the order that spreads a warp's 32 rows
+// over all banks: chunk i of thread r is physical chunk i ^ ((r >> 1) & 3).
+__device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, float f) {
+    const int x = (r >> 1) & 3;
+    for (int a = 0; a < nka; ++a) {
+        uint8_t *row = tile + a * 8192 + r * 64;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) scale_chunk_bf16(row + ((i ^ x) << 4), f);
     }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params P) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int dk = P.dk, dv = P.dv, H = P.H;
-    const Smem sp = smem_plan(dk, dv);
+    const int nka = dk / 32, nva = dv / 64;
+    // shared-memory offsets (scalars: nothing of the plan lives in local memory)
+    const Smem plan = smem_plan(dk, dv);
+    const uint32_t o_q = plan.q, o_k0 = plan.k0, o_k1 = plan.k1, o_v0 = plan.v0, o_v1 = plan.v1, o_s = plan.s;
     const uint32_t sbase = smem_u32(smem);
-    float *tab = reinterpret_cast<float *>(smem + sp.tab);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + sp.slot);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + sp.abort);
-    auto bar = [&](int i) -> uint32_t { return sbase + sp.bars + 8u * (uint32_t)i; };
+    const uint32_t bar0 = sbase + plan.bars;
+#define BAR(i) (bar0 + 8u * (uint32_t)(i))
+    float *tab = reinterpret_cast<float *>(smem + plan.tab);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + plan.slot);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + plan.abort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chain = blockIdx.x;
@@ -141,29 +160,30 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int nchunks = (int)((len + kC - 1) / kC);
     const int row0 = (int)rng.start;
     const float ld = __ldg(P.log_decay + h);
+    const float lam = expf(ld);
 
     if (threadIdx.x == 0) {
         if (!valid) record_status(GLA_ERR_DEVICE_ARG);
         *abort_flag = 0;
-        mbar_init(bar(B_QFULL), 1);
-        mbar_init(bar(B_QEMPTY), 1);
-        mbar_init(bar(B_KVFULL0), 1);
-        mbar_init(bar(B_KVFULL1), 1);
-        mbar_init(bar(B_KVEMPTY0), 1);
-        mbar_init(bar(B_KVEMPTY1), 1);
-        mbar_init(bar(B_AFULL), 1);
-        mbar_init(bar(B_PREP), kComputeThreads);
-        mbar_init(bar(B_SREADY), kComputeThreads);
-        mbar_init(bar(B_PFULL), kComputeThreads);
-        mbar_init(bar(B_OFULL), 1);
-        mbar_init(bar(B_OFREE), kComputeThreads);
-        mbar_init(bar(B_SFULL), 1);
-        mbar_init(bar(B_FINAL), 1);
+        mbar_init(BAR(B_QFULL), 1);
+        mbar_init(BAR(B_QEMPTY), 1);
+        mbar_init(BAR(B_KVFULL0), 1);
+        mbar_init(BAR(B_KVFULL1), 1);
+        mbar_init(BAR(B_KVEMPTY0), 1);
+        mbar_init(BAR(B_KVEMPTY1), 1);
+        mbar_init(BAR(B_AFULL), 1);
+        mbar_init(BAR(B_PREP), 4);
+        mbar_init(BAR(B_SREADY), 4);
+        mbar_init(BAR(B_PFULL), 4);
+        mbar_init(BAR(B_OFULL), 1);
+        mbar_init(BAR(B_OFREE), 4);
+        mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_FINAL), 1);
         fence_mbar_init();
     }
     if (threadIdx.x < kC + 4) tab[threadIdx.x] = (threadIdx.x <= kC) ? expf((float)threadIdx.x * ld) : 0.f;
     if (warp == kMmaWarp) {
-        tmem_alloc(sbase + sp.slot, kTmemCols);
+        tmem_alloc(sbase + plan.slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -179,23 +199,32 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            const int nka = dk / 32, nva = dv / 64;
+            tma_prefetch_desc(&tmO);
             const uint32_t kvbytes = (uint32_t)nka * 8192u + (uint32_t)nva * 16384u;
             const uint32_t qbytes = (uint32_t)nka * 8192u;
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = c & 1;
                 const int y = row0 + c * kC;
-                if (c >= 2) ok = mbar_wait(bar(B_KVEMPTY0 + s), ((c >> 1) - 1) & 1, abort_flag, kWaitBudgetNs);
+                if (c >= 2) ok = mbar_wait(BAR(B_KVEMPTY0 + s), ((c >> 1) - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
-                mbar_expect_tx(bar(B_KVFULL0 + s), kvbytes);
-                const uint32_t kdst = sbase + (s ? sp.k1 : sp.k0), vdst = sbase + (s ? sp.v1 : sp.v0);
-                for (int a = 0; a < nka; ++a) tma_load_2d(kdst + a * 8192u, &tmK, h * dk + 32 * a, y, bar(B_KVFULL0 + s));
-                for (int a = 0; a < nva; ++a) tma_load_2d(vdst + a * 16384u, &tmV, h * dv + 64 * a, y, bar(B_KVFULL0 + s));
-                if (c >= 1) ok = mbar_wait(bar(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                mbar_expect_tx(BAR(B_KVFULL0 + s), kvbytes);
+                const uint32_t kdst = sbase + (s ? o_k1 : o_k0), vdst = sbase + (s ? o_v1 : o_v0);
+                for (int a = 0; a < nka; ++a) tma_load_2d(kdst + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(B_KVFULL0 + s));
+                for (int a = 0; a < nva; ++a) tma_load_2d(vdst + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(B_KVFULL0 + s));
+                if (c + 1 < nchunks) {
+                    // warm L2 with the next chunk so its loads (Q waits for a free buffer) hit in L2
+                    const int yn = y + kC;
+                    for (int a = 0; a < nka; ++a) {
+                        tma_prefetch_l2_2d(&tmQ, h * dk + 32 * a, yn);
+                        tma_prefetch_l2_2d(&tmK, h * dk + 32 * a, yn);
+                    }
+                    for (int a = 0; a < nva; ++a) tma_prefetch_l2_2d(&tmV, h * dv + 64 * a, yn);
+                }
+                if (c >= 1) ok = mbar_wait(BAR(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
-                mbar_expect_tx(bar(B_QFULL), qbytes);
-                for (int a = 0; a < nka; ++a) tma_load_2d(sbase + sp.q + a * 8192u, &tmQ, h * dk + 32 * a, y, bar(B_QFULL));
+                mbar_expect_tx(BAR(B_QFULL), qbytes);
+                for (int a = 0; a < nka; ++a) tma_load_2d(sbase + o_q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_QFULL));
             }
             if (!ok) {
                 record_status(GLA_ERR_TIMEOUT);
@@ -210,13 +239,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint32_t id_pv = idesc_bf16(kC, dv, 0, 1);
             const uint32_t id_kv = idesc_bf16(kC, dv, 1, 1);
             const int ksteps_dk = dk / 16;
+            const uint32_t qbuf = sbase + o_q, sbuf = sbase + o_s;
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = c & 1;
-                const uint32_t kbuf = sbase + (s ? sp.k1 : sp.k0), vbuf = sbase + (s ? sp.v1 : sp.v0);
-                const uint32_t qbuf = sbase + sp.q, sbuf = sbase + sp.s;
-                ok = mbar_wait(bar(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
-                     mbar_wait(bar(B_QFULL), c & 1, abort_flag, kWaitBudgetNs);
+                const uint32_t kbuf = sbase + (s ? o_k1 : o_k0), vbuf = sbase + (s ? o_v1 : o_v0);
+                ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
+                     mbar_wait(BAR(B_QFULL), c & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 tc_fence_after();
                 // MMA1: A = Q K^T (both K-major, 64B swizzle; 2 K-steps per 32-column atom)
@@ -225,10 +254,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     mma_ss(tmem + kColA, smem_desc(qbuf + off, 16, 512, kSwizzle64B),
                            smem_desc(kbuf + off, 16, 512, kSwizzle64B), id_qk, kk > 0);
                 }
-                mma_commit(bar(B_AFULL));
-                ok = mbar_wait(bar(B_PREP), c & 1, abort_flag, kWaitBudgetNs) &&
-                     mbar_wait(bar(B_SREADY), c & 1, abort_flag, kWaitBudgetNs) &&
-                     (c == 0 || mbar_wait(bar(B_OFREE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
+                mma_commit(BAR(B_AFULL));
+                ok = mbar_wait(BAR(B_PREP), c & 1, abort_flag, kWaitBudgetNs) &&
+                     mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs) &&
+                     (c == 0 || mbar_wait(BAR(B_OFREE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
                 // MMA3: O = Q' S_{c-1} (A K-major 64B swizzle; B = S copy, MN-major 128B swizzle)
@@ -238,14 +267,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            smem_desc(sbuf + (uint32_t)kk * 2048u, (uint32_t)dk * 128u, 1024, kSwizzle128B), id_qs,
                            kk > 0);
                 }
+                mma_commit(BAR(B_QEMPTY));  // Q' is no longer needed: the next Q may land
                 // MMA4: S += K'^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
                            smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
                 }
-                mma_commit(bar(B_SFULL));
-                mma_commit(bar(B_QEMPTY));
-                ok = mbar_wait(bar(B_PFULL), c & 1, abort_flag, kWaitBudgetNs);
+                mma_commit(BAR(B_SFULL));
+                ok = mbar_wait(BAR(B_PFULL), c & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 tc_fence_after();
                 // MMA2: O += P V (A = P in TMEM, 8 columns per K-step of 16 tokens)
@@ -253,155 +282,204 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     mma_ts(tmem + kColO, tmem + kColA + (uint32_t)kk * 8u,
                            smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_pv, 1);
                 }
-                mma_commit(bar(B_OFULL));
-                mma_commit(bar(B_KVEMPTY0 + s));
+                mma_commit(BAR(B_OFULL));
             }
             if (!ok) {
                 record_status(GLA_ERR_TIMEOUT);
                 *abort_flag = 1;
             }
         }
-    } else if (warp < 8) {
-        // ------------------------------------------------------------ compute warps
-        const int t = threadIdx.x;          // 0..255
-        const int wg = t >> 7;              // column half
-        const int r = t & 127;              // TMEM lane = token row / state row
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int half_dv = dv / 2;
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ state warpgroup
+        const int r = threadIdx.x;                          // TMEM lane = dk row of S = tile row for prep
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const int64_t hstate = ((int64_t)seq * H + h) * dk * dv;
         bool ok = true;
         for (int c = 0; c <= nchunks && ok; ++c) {
             const int Lc = (c < nchunks) ? (int)((len - (int64_t)c * kC < kC) ? (len - (int64_t)c * kC) : kC) : 0;
-            // ---- state pass: S_{c-1} -> bf16 copy for MMA3, pre-scaled by lambda^L_c for MMA4 (or hT) ----
             if (c >= 1) {
-                ok = mbar_wait(bar(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 tc_fence_after();
             }
             const bool last = (c == nchunks);
             const float g = last ? 1.f : tab[Lc];
             if (r < dk) {
-                for (int j0 = wg * half_dv; j0 < (wg + 1) * half_dv; j0 += 32) {
-                    uint32_t v[32];
+                // two 32-column groups per step: both TMEM loads in flight before the first use
+                for (int j0 = 0; j0 < dv; j0 += 64) {
+                    uint32_t v[2][32];
                     if (c >= 1) {
-                        tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v);
+                        tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
+                        tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
                         tmem_wait_ld();
                     } else {
+                        const float4 *src = reinterpret_cast<const float4 *>(P.h0 + hstate + (int64_t)r * dv + j0);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            v[e] = __float_as_uint(P.h0 ? __ldg(P.h0 + hstate + (int64_t)r * dv + j0 + e) : 0.f);
+                        for (int e = 0; e < 16; ++e) {
+                            const float4 x = P.h0 ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v[e >> 3][4 * (e & 7)] = __float_as_uint(x.x);
+                            v[e >> 3][4 * (e & 7) + 1] = __float_as_uint(x.y);
+                            v[e >> 3][4 * (e & 7) + 2] = __float_as_uint(x.z);
+                            v[e >> 3][4 * (e & 7) + 3] = __float_as_uint(x.w);
+                        }
                     }
                     if (last) {
                         if (P.hT) {
                             float4 *dst = reinterpret_cast<float4 *>(P.hT + hstate + (int64_t)r * dv + j0);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                     __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                            for (int e = 0; e < 16; ++e)
+                                dst[e] = make_float4(__uint_as_float(v[e >> 3][4 * (e & 7)]),
+                                                     __uint_as_float(v[e >> 3][4 * (e & 7) + 1]),
+                                                     __uint_as_float(v[e >> 3][4 * (e & 7) + 2]),
+                                                     __uint_as_float(v[e >> 3][4 * (e & 7) + 3]));
                         }
                         continue;
                     }
-                    // bf16 copy into the MN-major, 128B-swizzled S tile
+                    // bf16 copy into the MN-major, 128B-swizzled S tile: one 64-column atom
+                    uint8_t *atom_row = smem + o_s + (uint32_t)(j0 >> 6) * (uint32_t)dk * 128u + (uint32_t)r * 128u;
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        const int j = j0 + 8 * q8;
-                        const uint32_t atom = (uint32_t)(j >> 6), chunk16 = (uint32_t)((j & 63) >> 3);
-                        uint8_t *dst = smem + sp.s + atom * (uint32_t)dk * 128u + (uint32_t)r * 128u +
-                                       ((chunk16 ^ (uint32_t)(r & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(dst) = make_uint4(
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 0]), __uint_as_float(v[8 * q8 + 1])),
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 2]), __uint_as_float(v[8 * q8 + 3])),
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 4]), __uint_as_float(v[8 * q8 + 5])),
-                            pack_bf16x2(__uint_as_float(v[8 * q8 + 6]), __uint_as_float(v[8 * q8 + 7])));
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                        *reinterpret_cast<uint4 *>(atom_row + (((uint32_t)q8 ^ (uint32_t)(r & 7)) << 4)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                       pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                       pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                       pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
                     }
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * g);
-                    tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v);
+                    for (int e = 0; e < 32; ++e) {
+                        v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * g);
+                        v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g);
+                    }
+                    tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
+                    tmem_st32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
                 }
             }
             if (last) break;
             tmem_wait_st();
             fence_async_shared();
             tc_fence_before();
-            mbar_arrive(bar(B_SREADY));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SREADY));
 
-            // ---- decay Q and K rows in place (after MMA1 has read them) ----
-            ok = mbar_wait(bar(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
+            // ---- decays of the Q and K rows, in place, once MMA1 has read them ----
+            ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
+            if (!ok) break;
+            tc_fence_after();
+            scale_row_sw64(smem + o_q, nka, r, tab[min(r + 1, kC)]);
+            scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < Lc) ? tab[Lc - 1 - r] : 0.f);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_PREP));
+        }
+        if (!ok) {
+            record_status(GLA_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------ output warpgroup
+        const int r = threadIdx.x - 128;                    // TMEM lane = token row
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int Lc = (int)((len - (int64_t)c * kC < kC) ? (len - (int64_t)c * kC) : kC);
+            const int s = c & 1;
+            // ---- decay mask: P = bf16(A .* D), D_rj = lambda^(r-j) for j <= r < Lc ----
+            ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
             {
-                const int s = c & 1;
-                const int nka = dk / 32;
-                if (wg == 0) {
-                    const float f = tab[min(r + 1, kC)];
-                    for (int a = 0; a < nka; ++a) scale_row_bf16(smem + sp.q + a * 8192 + r * 64, 64, f);
-                } else {
-                    const float f = (r < Lc) ? tab[Lc - 1 - r] : 0.f;
-                    uint8_t *kb = smem + (s ? sp.k1 : sp.k0);
-                    for (int a = 0; a < nka; ++a) scale_row_bf16(kb + a * 8192 + r * 64, 64, f);
-                }
-            }
-            fence_async_shared();
-            mbar_arrive(bar(B_PREP));
-
-            // ---- decay mask: P = bf16(A .* D), written over the first half of A's columns ----
-            {
-                uint32_t a0[32], a1[32];
-                const uint32_t acol = kColA + (uint32_t)(64 * wg);
-                tmem_ld32(tmem + lane_base + acol, a0);
-                tmem_ld32(tmem + lane_base + acol + 32, a1);
-                tmem_wait_ld();
-                uint32_t p[32];
                 const bool row_ok = r < Lc;
+                // 32-column blocks in increasing j: P block b (16 TMEM columns) only overwrites
+                // A columns this thread has already loaded.
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = 64 * wg + 2 * e;
-                    const int d0 = r - j, d1 = r - j - 1;
-                    const float f0 = (row_ok && d0 >= 0) ? tab[max(d0, 0)] : 0.f;
-                    const float f1 = (row_ok && d1 >= 0) ? tab[max(d1, 0)] : 0.f;
-                    p[e] = pack_bf16x2(__uint_as_float(a0[2 * e]) * f0, __uint_as_float(a0[2 * e + 1]) * f1);
-                }
+                for (int b = 0; b < 4; ++b) {
+                    uint32_t a[32], p[16];
+                    tmem_ld32(tmem + lane_base + kColA + (uint32_t)(32 * b), a);
+                    tmem_wait_ld();
+                    // walk j downwards from 32b+31: lambda^(r-j) grows by one factor of lambda per step
+                    const int dtop = r - (32 * b + 31);
+                    float f = tab[max(dtop, 0)];
+                    float dec[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = 64 * wg + 32 + 2 * e;
-                    const int d0 = r - j, d1 = r - j - 1;
-                    const float f0 = (row_ok && d0 >= 0) ? tab[max(d0, 0)] : 0.f;
-                    const float f1 = (row_ok && d1 >= 0) ? tab[max(d1, 0)] : 0.f;
-                    p[16 + e] = pack_bf16x2(__uint_as_float(a1[2 * e]) * f0, __uint_as_float(a1[2 * e + 1]) * f1);
+                    for (int e = 31; e >= 0; --e) {
+                        const bool on = row_ok && (dtop + (31 - e) >= 0);
+                        dec[e] = on ? f : 0.f;
+                        f = on ? f * lam : f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        p[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * dec[2 * e],
+                                           __uint_as_float(a[2 * e + 1]) * dec[2 * e + 1]);
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                        ::"r"(tmem + lane_base + kColA + (uint32_t)(16 * b)), "r"(p[0]), "r"(p[1]), "r"(p[2]),
+                          "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7]), "r"(p[8]), "r"(p[9]), "r"(p[10]),
+                          "r"(p[11]), "r"(p[12]), "r"(p[13]), "r"(p[14]), "r"(p[15])
+                        : "memory");
                 }
-                // every compute thread has read its A columns before any P column is written
-                named_bar_sync(1, kComputeThreads);
-                tmem_st32(tmem + lane_base + kColA + (uint32_t)(32 * wg), p);
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_PFULL));
 
-            // ---- output epilogue: O (f32, TMEM) -> bf16 rows of out ----
-            ok = mbar_wait(bar(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
+            // ---- output epilogue ----
+            ok = mbar_wait(BAR(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
-            {
-                __nv_bfloat16 *orow = P.out + ((int64_t)(row0 + (int64_t)c * kC + r) * H + h) * dv;
-                for (int j0 = wg * half_dv; j0 < (wg + 1) * half_dv; j0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v);
-                    tmem_wait_ld();
-                    if (r < Lc) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + j0);
+            const bool full = (Lc == kC);
+            uint8_t *stage = smem + (s ? o_v1 : o_v0);  // MMA2 and MMA4 are done with this V tile
+            __nv_bfloat16 *orow = P.out + ((int64_t)(row0 + (int64_t)c * kC + r) * H + h) * dv;
+            for (int j0 = 0; j0 < dv; j0 += 64) {
+                uint32_t v[2][32];
+                tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
+                tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0 + 32u, v[1]);
+                tmem_wait_ld();
+                if (j0 + 64 >= dv) {  // last TMEM read of O for this chunk: MMA3 of the next chunk may start
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(B_OFREE));
+                }
+                if (full) {
+                    // bf16 row into the 128B-swizzled [128 x 64] atom, the layout the O tensor map stores
+                    uint8_t *atom_row = stage + (uint32_t)(j0 >> 6) * 16384u + (uint32_t)r * 128u;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[8 * e + 0]), __uint_as_float(v[8 * e + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7])));
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                        *reinterpret_cast<uint4 *>(atom_row + (((uint32_t)q8 ^ (uint32_t)(r & 7)) << 4)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                       pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                       pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                       pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                    }
+                } else if (r < Lc) {
+                    // a partial chunk is followed by another sequence's rows: plain stores, row by row
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + j0);
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                        dst[q8] = make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                             pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                             pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                             pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(B_OFREE));
+            if (full) fence_async_shared();
+            named_bar_sync(1, 128);
+            if (r == 0) {
+                if (full) {
+                    const int y = row0 + c * kC;
+                    for (int a = 0; a < nva; ++a) tma_store_2d(&tmO, h * dv + 64 * a, y, sbase + (s ? o_v1 : o_v0) + a * 16384u);
+                    bulk_commit();
+                    bulk_wait_read0();  // the stage may be refilled once the store has read it
+                }
+                mbar_arrive(BAR(B_KVEMPTY0 + s));
+            }
         }
+        if (r == 0) bulk_wait0();  // all output stores complete before the CTA exits
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
             *abort_flag = 1;
@@ -414,12 +492,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (warp == kMmaWarp) {
         tc_fence_after();
         if (*abort_flag) {
-            if (lane == 0) mma_commit(bar(B_FINAL));
+            if (lane == 0) mma_commit(BAR(B_FINAL));
             __syncwarp();
-            mbar_wait(bar(B_FINAL), 0, nullptr, kWaitBudgetNs);
+            mbar_wait(BAR(B_FINAL), 0, nullptr, kWaitBudgetNs);
         }
         tmem_dealloc(tmem, kTmemCols);
     }
+#undef BAR
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -467,10 +546,11 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
     const Smem sp = smem_plan(dk, dv);
     const size_t bytes = sp.total + 1024;  // + alignment slack
@@ -491,7 +571,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.dv = dv;
     const long long chains = (long long)nseq * H;
     if (chains > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    gla_tc_chunk_kernel<<<(unsigned)chains, kThreads, bytes, st>>>(mq, mk, mv, p);
+    gla_tc_chunk_kernel<<<(unsigned)chains, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }

@@ -76,7 +76,7 @@ struct Params {
 
 // Shared memory plan (bytes from the 1024-aligned base).
 struct Smem {
-    uint32_t q, k0, k1, v0, v1, s, tab, bars, slot, abort, total;
+    uint32_t q, k0, k1, v0, v1, s, tab, utab, bars, slot, abort, total;
 };
 
 __host__ __device__ inline Smem smem_plan(int dk, int dv) {
@@ -90,7 +90,8 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     p.v1 = p.v0 + vv;
     p.s = p.v1 + vv;
     p.tab = p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64);
-    p.bars = p.tab + 132 * 4;
+    p.utab = p.tab + 132 * 4;
+    p.bars = p.utab + 128 * 4;
     p.bars = (p.bars + 7u) & ~7u;
     p.slot = p.bars + 16 * 8;
     p.abort = p.slot + 4;
@@ -99,8 +100,8 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 }
 
 // barrier indices
-enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_PREP, B_SREADY, B_PFULL,
-       B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_COUNT };
+enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP, B_SREADY,
+       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -146,7 +147,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + plan.bars;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
-    float *tab = reinterpret_cast<float *>(smem + plan.tab);
+    float *tab = reinterpret_cast<float *>(smem + plan.tab);    // lambda^n,      n = 0..128
+    float *utab = reinterpret_cast<float *>(smem + plan.utab);  // lambda^-(j+1), j = 0..127 (factored mode)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + plan.slot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + plan.abort);
 
@@ -161,6 +163,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int row0 = (int)rng.start;
     const float ld = __ldg(P.log_decay + h);
     const float lam = expf(ld);
+    // Factored decay: lambda^(i-j) = lambda^(i+1) * lambda^-(j+1).  The row factor is applied to O in
+    // the epilogue and the column factor to P in the mask, so Q needs no rescaled copy and MMA1/MMA3
+    // run on the tiles as loaded.  Used while lambda^-128 stays far from overflow (lambda >= e^-0.3);
+    // stronger decays take the direct form (Q rows rescaled in place, per-element decay in the mask).
+    const bool fact = ld >= -0.3f;
 
     if (threadIdx.x == 0) {
         if (!valid) record_status(GLA_ERR_DEVICE_ARG);
@@ -172,7 +179,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_KVEMPTY0), 1);
         mbar_init(BAR(B_KVEMPTY1), 1);
         mbar_init(BAR(B_AFULL), 1);
-        mbar_init(BAR(B_PREP), 4);
+        mbar_init(BAR(B_QPREP), 4);
+        mbar_init(BAR(B_KPREP), 4);
         mbar_init(BAR(B_SREADY), 4);
         mbar_init(BAR(B_PFULL), 4);
         mbar_init(BAR(B_OFULL), 1);
@@ -182,6 +190,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         fence_mbar_init();
     }
     if (threadIdx.x < kC + 4) tab[threadIdx.x] = (threadIdx.x <= kC) ? expf((float)threadIdx.x * ld) : 0.f;
+    if (threadIdx.x < kC) utab[threadIdx.x] = fact ? expf(-(float)(threadIdx.x + 1) * ld) : 0.f;
     if (warp == kMmaWarp) {
         tmem_alloc(sbase + plan.slot, kTmemCols);
         tmem_relinquish();
@@ -212,6 +221,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const uint32_t kdst = sbase + (s ? o_k1 : o_k0), vdst = sbase + (s ? o_v1 : o_v0);
                 for (int a = 0; a < nka; ++a) tma_load_2d(kdst + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(B_KVFULL0 + s));
                 for (int a = 0; a < nva; ++a) tma_load_2d(vdst + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(B_KVFULL0 + s));
+                if (c >= 1) ok = mbar_wait(BAR(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                if (!ok) break;
+                mbar_expect_tx(BAR(B_QFULL), qbytes);
+                for (int a = 0; a < nka; ++a) tma_load_2d(sbase + o_q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_QFULL));
                 if (c + 1 < nchunks) {
                     // warm L2 with the next chunk so its loads (Q waits for a free buffer) hit in L2
                     const int yn = y + kC;
@@ -221,10 +234,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     }
                     for (int a = 0; a < nva; ++a) tma_prefetch_l2_2d(&tmV, h * dv + 64 * a, yn);
                 }
-                if (c >= 1) ok = mbar_wait(BAR(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
-                if (!ok) break;
-                mbar_expect_tx(BAR(B_QFULL), qbytes);
-                for (int a = 0; a < nka; ++a) tma_load_2d(sbase + o_q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_QFULL));
             }
             if (!ok) {
                 record_status(GLA_ERR_TIMEOUT);
@@ -255,19 +264,23 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            smem_desc(kbuf + off, 16, 512, kSwizzle64B), id_qk, kk > 0);
                 }
                 mma_commit(BAR(B_AFULL));
-                ok = mbar_wait(BAR(B_PREP), c & 1, abort_flag, kWaitBudgetNs) &&
+                ok = (fact || mbar_wait(BAR(B_QPREP), c & 1, abort_flag, kWaitBudgetNs)) &&
                      mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs) &&
                      (c == 0 || mbar_wait(BAR(B_OFREE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
-                // MMA3: O = Q' S_{c-1} (A K-major 64B swizzle; B = S copy, MN-major 128B swizzle)
+                // MMA3: O = Q S_{c-1} (factored) or Q' S_{c-1} (direct); A K-major 64B swizzle,
+                // B = S copy, MN-major 128B swizzle
                 for (int kk = 0; kk < ksteps_dk; ++kk) {
                     const uint32_t aoff = (uint32_t)(kk >> 1) * 8192u + (uint32_t)(kk & 1) * 32u;
                     mma_ss(tmem + kColO, smem_desc(qbuf + aoff, 16, 512, kSwizzle64B),
                            smem_desc(sbuf + (uint32_t)kk * 2048u, (uint32_t)dk * 128u, 1024, kSwizzle128B), id_qs,
                            kk > 0);
                 }
-                mma_commit(BAR(B_QEMPTY));  // Q' is no longer needed: the next Q may land
+                mma_commit(BAR(B_QEMPTY));  // Q is no longer needed: the next Q may land
+                ok = mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs);
+                if (!ok) break;
+                tc_fence_after();
                 // MMA4: S += K'^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
@@ -366,11 +379,16 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
-            scale_row_sw64(smem + o_q, nka, r, tab[min(r + 1, kC)]);
+            if (!fact) {
+                scale_row_sw64(smem + o_q, nka, r, tab[min(r + 1, kC)]);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_QPREP));
+            }
             scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < Lc) ? tab[Lc - 1 - r] : 0.f);
             fence_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PREP));
+            if (lane == 0) mbar_arrive(BAR(B_KPREP));
         }
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
@@ -397,15 +415,24 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     uint32_t a[32], p[16];
                     tmem_ld32(tmem + lane_base + kColA + (uint32_t)(32 * b), a);
                     tmem_wait_ld();
-                    // walk j downwards from 32b+31: lambda^(r-j) grows by one factor of lambda per step
-                    const int dtop = r - (32 * b + 31);
-                    float f = tab[max(dtop, 0)];
                     float dec[32];
+                    if (fact) {
+                        // column factor lambda^-(j+1) on the causal part (row factor comes in the epilogue)
 #pragma unroll
-                    for (int e = 31; e >= 0; --e) {
-                        const bool on = row_ok && (dtop + (31 - e) >= 0);
-                        dec[e] = on ? f : 0.f;
-                        f = on ? f * lam : f;
+                        for (int e = 0; e < 32; ++e) {
+                            const int j = 32 * b + e;
+                            dec[e] = (row_ok && j <= r) ? utab[j] : 0.f;
+                        }
+                    } else {
+                        // walk j downwards from 32b+31: lambda^(r-j) grows by one factor of lambda per step
+                        const int dtop = r - (32 * b + 31);
+                        float f = tab[max(dtop, 0)];
+#pragma unroll
+                        for (int e = 31; e >= 0; --e) {
+                            const bool on = row_ok && (dtop + (31 - e) >= 0);
+                            dec[e] = on ? f : 0.f;
+                            f = on ? f * lam : f;
+                        }
                     }
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -430,6 +457,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (!ok) break;
             tc_fence_after();
             const bool full = (Lc == kC);
+            const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1) in the factored form
             uint8_t *stage = smem + (s ? o_v1 : o_v0);  // MMA2 and MMA4 are done with this V tile
             __nv_bfloat16 *orow = P.out + ((int64_t)(row0 + (int64_t)c * kC + r) * H + h) * dv;
             for (int j0 = 0; j0 < dv; j0 += 64) {
@@ -441,6 +469,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(B_OFREE));
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * grow);
+                    v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * grow);
                 }
                 if (full) {
                     // bf16 row into the 128B-swizzled [128 x 64] atom, the layout the O tensor map stores

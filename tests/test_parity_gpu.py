@@ -114,6 +114,18 @@ def test_decay_extremes():
     assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
 
 
+@pytest.mark.parametrize("lds", [[-0.29, -0.31, -0.5, -2.0], [-1e-4, -0.05, -0.2999, -5.0]])
+def test_bf16_mild_and_strong_decays(lds):
+    """Both decay forms of the tensor-core kernel (factored for lambda >= e^-0.3, direct below)."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=400, H=4, h0_std=0.1)
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=11))
+    d["log_decay"] = torch.tensor(lds, device="cuda")
+    out, hT = run_prefill(d, 128)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(out.float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
+
+
 # ---- invariants on the GPU path ----
 def test_deterministic_and_causal():
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=400, H=4, h0_std=0.02)

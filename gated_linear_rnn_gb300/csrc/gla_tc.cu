@@ -21,17 +21,19 @@
 //
 // Warp roles (320 threads):
 //   warps 0-3  "state" warpgroup: thread t owns TMEM lane t (a dk row of S).
-//              Per chunk: state pass (read S_{c-1} from TMEM, write its bf16
-//              copy for MMA3, pre-scale it by lambda^L for MMA4), then the
-//              decays of the Q and K rows in place (after MMA1 read them).
+//              Per chunk: state pass (read the state accumulator from TMEM,
+//              finish S_{c-1}, write its bf16 copy for MMA3 and the f32 value
+//              back for MMA4), then the K row decays in place (and, for strong
+//              decays, the Q row decays).
 //   warps 4-7  "output" warpgroup: thread t owns TMEM lane t - 128 (a token
-//              row).  Per chunk: decay mask A -> P, then the output epilogue:
-//              O (TMEM) -> bf16 into the chunk's V tile (free once MMA2 and
-//              MMA4 are done) -> TMA store, which is also what releases the
-//              chunk's K/V stage to the producer.
+//              row).  Per chunk: mask A -> P, then the output epilogue:
+//              O (TMEM) -> bf16, staged in the chunk's V tile (free once MMA2
+//              and MMA4 are done).
 //   warp 8     TMA producer: Q (single buffer), K and V (double buffer), plus
 //              an L2 prefetch of the next chunk.
 //   warp 9     MMA issuer and TMEM owner.
+//   warp 10    TMA store of the staged O tiles; hands each K/V stage back to
+//              the producer once its store has read the tile.
 // Hand-offs are mbarriers; every wait is bounded (see sm100_ptx.cuh) and a
 // timeout is recorded as GLA_ERR_TIMEOUT in the device status word.
 //
@@ -56,9 +58,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kC = 128;              // chunk length (MMA M and the token K extent)
-constexpr int kThreads = 320;        // 8 compute warps + producer + MMA warp
+constexpr int kThreads = 352;        // 8 compute warps + producer + MMA warp + store warp
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kStoreWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;        // O accumulator  [0, dv)
 constexpr uint32_t kColS = 192;      // state          [192, 192 + dv)
@@ -93,7 +96,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     p.utab = p.tab + 132 * 4;
     p.bars = p.utab + 128 * 4;
     p.bars = (p.bars + 7u) & ~7u;
-    p.slot = p.bars + 16 * 8;
+    p.slot = p.bars + 24 * 8;
     p.abort = p.slot + 4;
     p.total = p.abort + 4;
     return p;
@@ -101,7 +104,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 
 // barrier indices
 enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP, B_SREADY,
-       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_COUNT };
+       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_OSTAGED0, B_OSTAGED1, B_FINAL, B_COUNT };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -148,7 +151,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const uint32_t bar0 = sbase + plan.bars;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
     float *tab = reinterpret_cast<float *>(smem + plan.tab);    // lambda^n,      n = 0..128
-    float *utab = reinterpret_cast<float *>(smem + plan.utab);  // lambda^-(j+1), j = 0..127 (factored mode)
+    float *utab = reinterpret_cast<float *>(smem + plan.utab);  // lambda^-(j+1), j = 0..127 (factored form)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + plan.slot);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + plan.abort);
 
@@ -163,11 +166,17 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int row0 = (int)rng.start;
     const float ld = __ldg(P.log_decay + h);
     const float lam = expf(ld);
-    // Factored decay: lambda^(i-j) = lambda^(i+1) * lambda^-(j+1).  The row factor is applied to O in
-    // the epilogue and the column factor to P in the mask, so Q needs no rescaled copy and MMA1/MMA3
-    // run on the tiles as loaded.  Used while lambda^-128 stays far from overflow (lambda >= e^-0.3);
-    // stronger decays take the direct form (Q rows rescaled in place, per-element decay in the mask).
+    // Factored decay: lambda^(i-j) = lambda^(i+1) * lambda^-(j+1).  K rows are scaled by lambda^-(j+1)
+    // once (K''), which serves both A = Q K''^T (the decay mask becomes a plain causal mask) and the
+    // state update S_c = lambda^L (S_{c-1} + K''^T V); the row factor lambda^(i+1) is applied to O in
+    // the epilogue, so Q needs no rescaled copy.  Used while lambda^-128 stays far from overflow
+    // (lambda >= e^-0.3); stronger decays take the direct form: Q rows scaled by lambda^(i+1), K rows
+    // by lambda^(L-1-j), per-element decay in the mask, state pre-scaled by lambda^L.
     const bool fact = ld >= -0.3f;
+    auto chunk_len = [&](int c) -> int {
+        const int64_t rem = len - (int64_t)c * kC;
+        return (int)(rem < kC ? rem : kC);
+    };
 
     if (threadIdx.x == 0) {
         if (!valid) record_status(GLA_ERR_DEVICE_ARG);
@@ -186,6 +195,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_OFULL), 1);
         mbar_init(BAR(B_OFREE), 4);
         mbar_init(BAR(B_SFULL), 1);
+        mbar_init(BAR(B_OSTAGED0), 4);
+        mbar_init(BAR(B_OSTAGED1), 4);
         mbar_init(BAR(B_FINAL), 1);
         fence_mbar_init();
     }
@@ -208,7 +219,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            tma_prefetch_desc(&tmO);
             const uint32_t kvbytes = (uint32_t)nka * 8192u + (uint32_t)nva * 16384u;
             const uint32_t qbytes = (uint32_t)nka * 8192u;
             bool ok = true;
@@ -240,6 +250,32 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 *abort_flag = 1;
             }
         }
+    } else if (warp == kStoreWarp) {
+        // ------------------------------------------------------------ output stores
+        // O of chunk c is staged (bf16, 128B swizzle) in the chunk's V tile; this warp stores it with
+        // TMA and, once the store has read the tile, hands the K/V stage back to the producer.
+        if (lane == 0 && nchunks > 0) {
+            tma_prefetch_desc(&tmO);
+            bool ok = true;
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int s = c & 1;
+                ok = mbar_wait(BAR(B_OSTAGED0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs);
+                if (!ok) break;
+                if (chunk_len(c) == kC) {
+                    const int y = row0 + c * kC;
+                    const uint32_t src = sbase + (s ? o_v1 : o_v0);
+                    for (int a = 0; a < nva; ++a) tma_store_2d(&tmO, h * dv + 64 * a, y, src + a * 16384u);
+                    bulk_commit();
+                    bulk_wait_read0();
+                }
+                mbar_arrive(BAR(B_KVEMPTY0 + s));
+            }
+            bulk_wait0();  // every output store has landed before the CTA exits
+            if (!ok) {
+                record_status(GLA_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && nchunks > 0) {
@@ -254,10 +290,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const int s = c & 1;
                 const uint32_t kbuf = sbase + (s ? o_k1 : o_k0), vbuf = sbase + (s ? o_v1 : o_v0);
                 ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
-                     mbar_wait(BAR(B_QFULL), c & 1, abort_flag, kWaitBudgetNs);
+                     mbar_wait(BAR(B_QFULL), c & 1, abort_flag, kWaitBudgetNs) &&
+                     (!fact || mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
-                // MMA1: A = Q K^T (both K-major, 64B swizzle; 2 K-steps per 32-column atom)
+                // MMA1: A = Q K^T, K'' in the factored form (both K-major, 64B swizzle; 2 K-steps per atom)
                 for (int kk = 0; kk < ksteps_dk; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 1) * 8192u + (uint32_t)(kk & 1) * 32u;
                     mma_ss(tmem + kColA, smem_desc(qbuf + off, 16, 512, kSwizzle64B),
@@ -278,10 +315,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            kk > 0);
                 }
                 mma_commit(BAR(B_QEMPTY));  // Q is no longer needed: the next Q may land
-                ok = mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs);
-                if (!ok) break;
-                tc_fence_after();
-                // MMA4: S += K'^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
+                if (!fact) {
+                    ok = mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // MMA4: S += K~^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
                            smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
@@ -308,15 +347,28 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const int64_t hstate = ((int64_t)seq * H + h) * dk * dv;
         bool ok = true;
+        // factored form: K''_c rows = lambda^-(j+1) k_j (zero beyond the chunk), as soon as K_c lands
+        auto prep_k_fact = [&](int c) -> bool {
+            if (!mbar_wait(BAR(B_KVFULL0 + (c & 1)), (c >> 1) & 1, abort_flag, kWaitBudgetNs)) return false;
+            scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < chunk_len(c)) ? utab[r] : 0.f);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_KPREP));
+            return true;
+        };
+        if (fact && nchunks > 0) ok = prep_k_fact(0);
         for (int c = 0; c <= nchunks && ok; ++c) {
-            const int Lc = (c < nchunks) ? (int)((len - (int64_t)c * kC < kC) ? (len - (int64_t)c * kC) : kC) : 0;
             if (c >= 1) {
                 ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 tc_fence_after();
             }
             const bool last = (c == nchunks);
-            const float g = last ? 1.f : tab[Lc];
+            // factored: TMEM holds S_{c-2} + K''^T V, S_{c-1} = lambda^L(c-1) * that; copy and TMEM both get it.
+            // direct:   TMEM holds S_{c-1}; the copy is S_{c-1}, TMEM gets lambda^L(c) S_{c-1} for MMA4.
+            const float g_prev = (fact && c >= 1) ? tab[chunk_len(c - 1)] : 1.f;
+            const float g_copy = g_prev;
+            const float g_tmem = fact ? g_prev : (last ? 1.f : tab[chunk_len(c)]);
             if (r < dk) {
                 // two 32-column groups per step: both TMEM loads in flight before the first use
                 for (int j0 = 0; j0 < dv; j0 += 64) {
@@ -335,6 +387,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             v[e >> 3][4 * (e & 7) + 2] = __float_as_uint(x.z);
                             v[e >> 3][4 * (e & 7) + 3] = __float_as_uint(x.w);
                         }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * g_copy);
+                        v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g_copy);
                     }
                     if (last) {
                         if (P.hT) {
@@ -359,10 +416,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                        pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
                                        pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
                     }
+                    if (g_tmem != g_copy || c == 0) {
+                        const float gt = g_tmem / (c == 0 ? 1.f : g_copy);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * g);
-                        v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g);
+                        for (int e = 0; e < 32; ++e) {
+                            v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * gt);
+                            v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * gt);
+                        }
                     }
                     tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
                     tmem_st32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
@@ -375,20 +435,23 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SREADY));
 
-            // ---- decays of the Q and K rows, in place, once MMA1 has read them ----
-            ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
-            if (!ok) break;
-            tc_fence_after();
-            if (!fact) {
+            if (fact) {
+                if (c + 1 < nchunks) ok = prep_k_fact(c + 1);
+            } else {
+                // direct form: decays of the Q and K rows, in place, once MMA1 has read them
+                ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
+                if (!ok) break;
+                tc_fence_after();
+                const int Lc = chunk_len(c);
                 scale_row_sw64(smem + o_q, nka, r, tab[min(r + 1, kC)]);
                 fence_async_shared();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_QPREP));
+                scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < Lc) ? tab[Lc - 1 - r] : 0.f);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_KPREP));
             }
-            scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < Lc) ? tab[Lc - 1 - r] : 0.f);
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_KPREP));
         }
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
@@ -398,11 +461,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // ------------------------------------------------------------ output warpgroup
         const int r = threadIdx.x - 128;                    // TMEM lane = token row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int Lc = (int)((len - (int64_t)c * kC < kC) ? (len - (int64_t)c * kC) : kC);
+            const int Lc = chunk_len(c);
             const int s = c & 1;
-            // ---- decay mask: P = bf16(A .* D), D_rj = lambda^(r-j) for j <= r < Lc ----
+            // ---- mask: P = bf16(A .* D) ----
             ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
@@ -415,16 +479,18 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     uint32_t a[32], p[16];
                     tmem_ld32(tmem + lane_base + kColA + (uint32_t)(32 * b), a);
                     tmem_wait_ld();
-                    float dec[32];
                     if (fact) {
-                        // column factor lambda^-(j+1) on the causal part (row factor comes in the epilogue)
+                        // the decay already sits in K'' and in the epilogue's row factor: causal mask only
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int j = 32 * b + e;
-                            dec[e] = (row_ok && j <= r) ? utab[j] : 0.f;
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = 32 * b + 2 * e;
+                            const float x0 = (row_ok && j <= r) ? __uint_as_float(a[2 * e]) : 0.f;
+                            const float x1 = (row_ok && j + 1 <= r) ? __uint_as_float(a[2 * e + 1]) : 0.f;
+                            p[e] = pack_bf16x2(x0, x1);
                         }
                     } else {
-                        // walk j downwards from 32b+31: lambda^(r-j) grows by one factor of lambda per step
+                        // D_rj = lambda^(r-j): walk j downwards from 32b+31, one factor of lambda per step
+                        float dec[32];
                         const int dtop = r - (32 * b + 31);
                         float f = tab[max(dtop, 0)];
 #pragma unroll
@@ -433,11 +499,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             dec[e] = on ? f : 0.f;
                             f = on ? f * lam : f;
                         }
-                    }
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        p[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * dec[2 * e],
-                                           __uint_as_float(a[2 * e + 1]) * dec[2 * e + 1]);
+                        for (int e = 0; e < 16; ++e)
+                            p[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * dec[2 * e],
+                                               __uint_as_float(a[2 * e + 1]) * dec[2 * e + 1]);
+                    }
                     asm volatile(
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                         "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -452,12 +518,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
 
-            // ---- output epilogue ----
+            // ---- output epilogue: O -> bf16 -> staged in the chunk's V tile (the store warp writes it) ----
             ok = mbar_wait(BAR(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
             const bool full = (Lc == kC);
-            const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1) in the factored form
             uint8_t *stage = smem + (s ? o_v1 : o_v0);  // MMA2 and MMA4 are done with this V tile
             __nv_bfloat16 *orow = P.out + ((int64_t)(row0 + (int64_t)c * kC + r) * H + h) * dv;
             for (int j0 = 0; j0 < dv; j0 += 64) {
@@ -500,19 +565,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     }
                 }
             }
-            if (full) fence_async_shared();
-            named_bar_sync(1, 128);
-            if (r == 0) {
-                if (full) {
-                    const int y = row0 + c * kC;
-                    for (int a = 0; a < nva; ++a) tma_store_2d(&tmO, h * dv + 64 * a, y, sbase + (s ? o_v1 : o_v0) + a * 16384u);
-                    bulk_commit();
-                    bulk_wait_read0();  // the stage may be refilled once the store has read it
-                }
-                mbar_arrive(BAR(B_KVEMPTY0 + s));
-            }
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_OSTAGED0 + s));
         }
-        if (r == 0) bulk_wait0();  // all output stores complete before the CTA exits
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
             *abort_flag = 1;

@@ -67,14 +67,27 @@ constexpr uint32_t kColO = 0;        // O accumulator  [0, dv)
 constexpr uint32_t kColS = 192;      // state          [192, 192 + dv)
 constexpr uint32_t kColA = 384;      // A = Q K^T      [384, 512); P aliases [384, 448)
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;  // 4 s per wait
+constexpr int kL2Ahead = 2;          // chunks of L2 prefetch ahead of the current load
+
+// Launch modes.  A long dense sequence with few (sequence, head) chains is cut into nseg
+// segments of seg_chunks chunks: pass 1 (kStateOnly) computes every segment's end state from a zero
+// start, a small scan turns those into the segment start states, and pass 2 (kSegmented) runs the
+// full forward of every segment from its start state.
+enum Mode : int { kWhole = 0, kStateOnly = 1, kSegmented = 2 };
 
 struct Params {
     const float *log_decay;
-    const float *h0;
+    const float *h0;       // [nseq, H, dk, dv] or null
     __nv_bfloat16 *out;
-    float *hT;
+    float *hT;             // [nseq, H, dk, dv] or null
     const int32_t *cu;
     int T, H, dk, dv;
+    int mode;              // Mode
+    int nseg;              // segments per chain (1 for kWhole)
+    int seg_chunks;        // chunks per segment (segmented modes)
+    int grid_seg;          // segments per chain in this launch (nseg - 1 for kStateOnly)
+    const float *seg_h0;   // kSegmented: start states of segments 1..nseg-1, [chains, nseg-1, dk, dv]
+    float *seg_end;        // kStateOnly: end states of segments 0..nseg-2 from zero, [chains, nseg-1, dk, dv]
 };
 
 // Shared memory plan (bytes from the 1024-aligned base).
@@ -156,14 +169,32 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + plan.abort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chain = blockIdx.x;
+    const int chain = blockIdx.x / P.grid_seg, seg = blockIdx.x % P.grid_seg;
     const int seq = chain / H, h = chain % H;
+    const bool state_only = P.mode == kStateOnly;
 
     SeqRange rng;
     const bool valid = seq_range(seq, P.T, P.cu, rng);
-    const int64_t len = valid ? rng.len : 0;
+    int64_t len = valid ? rng.len : 0;
+    int64_t start = rng.start;
+    if (P.mode != kWhole) {  // one segment of a dense sequence
+        const int64_t s0 = (int64_t)seg * P.seg_chunks * kC;
+        start += s0;
+        len = (len - s0 < (int64_t)P.seg_chunks * kC) ? len - s0 : (int64_t)P.seg_chunks * kC;
+    }
     const int nchunks = (int)((len + kC - 1) / kC);
-    const int row0 = (int)rng.start;
+    const int row0 = (int)start;
+    // where the chain segment's initial state comes from and where its final state goes (null: zeros / none)
+    const int64_t sz_state = (int64_t)P.dk * P.dv;
+    const float *init_state = P.h0 ? P.h0 + ((int64_t)seq * H + h) * sz_state : nullptr;
+    float *final_state = P.hT ? P.hT + ((int64_t)seq * H + h) * sz_state : nullptr;
+    if (P.mode == kStateOnly) {
+        init_state = nullptr;
+        final_state = P.seg_end + ((int64_t)chain * (P.nseg - 1) + seg) * sz_state;
+    } else if (P.mode == kSegmented) {
+        if (seg > 0) init_state = P.seg_h0 + ((int64_t)chain * (P.nseg - 1) + seg - 1) * sz_state;
+        if (seg < P.nseg - 1) final_state = nullptr;
+    }
     const float ld = __ldg(P.log_decay + h);
     const float lam = expf(ld);
     // Factored decay: lambda^(i-j) = lambda^(i+1) * lambda^-(j+1).  K rows are scaled by lambda^-(j+1)
@@ -231,15 +262,20 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const uint32_t kdst = sbase + (s ? o_k1 : o_k0), vdst = sbase + (s ? o_v1 : o_v0);
                 for (int a = 0; a < nka; ++a) tma_load_2d(kdst + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(B_KVFULL0 + s));
                 for (int a = 0; a < nva; ++a) tma_load_2d(vdst + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(B_KVFULL0 + s));
-                if (c >= 1) ok = mbar_wait(BAR(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
-                if (!ok) break;
-                mbar_expect_tx(BAR(B_QFULL), qbytes);
-                for (int a = 0; a < nka; ++a) tma_load_2d(sbase + o_q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_QFULL));
-                if (c + 1 < nchunks) {
-                    // warm L2 with the next chunk so its loads (Q waits for a free buffer) hit in L2
-                    const int yn = y + kC;
+                if (!state_only) {
+                    if (c >= 1) ok = mbar_wait(BAR(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                    if (!ok) break;
+                    mbar_expect_tx(BAR(B_QFULL), qbytes);
+                    for (int a = 0; a < nka; ++a)
+                        tma_load_2d(sbase + o_q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_QFULL));
+                }
+                // Warm L2 two chunks ahead: the shared-memory stages only allow loads one chunk
+                // ahead, which is shorter than the HBM latency under load, so the loads that do
+                // go out should find their lines already in L2.
+                for (int cp = (c == 0 ? 1 : c + kL2Ahead); cp <= c + kL2Ahead && cp < nchunks; ++cp) {
+                    const int yn = row0 + cp * kC;
                     for (int a = 0; a < nka; ++a) {
-                        tma_prefetch_l2_2d(&tmQ, h * dk + 32 * a, yn);
+                        if (!state_only) tma_prefetch_l2_2d(&tmQ, h * dk + 32 * a, yn);
                         tma_prefetch_l2_2d(&tmK, h * dk + 32 * a, yn);
                     }
                     for (int a = 0; a < nva; ++a) tma_prefetch_l2_2d(&tmV, h * dv + 64 * a, yn);
@@ -254,7 +290,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // ------------------------------------------------------------ output stores
         // O of chunk c is staged (bf16, 128B swizzle) in the chunk's V tile; this warp stores it with
         // TMA and, once the store has read the tile, hands the K/V stage back to the producer.
-        if (lane == 0 && nchunks > 0) {
+        if (lane == 0 && nchunks > 0 && !state_only) {
             tma_prefetch_desc(&tmO);
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
@@ -289,6 +325,21 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = c & 1;
                 const uint32_t kbuf = sbase + (s ? o_k1 : o_k0), vbuf = sbase + (s ? o_v1 : o_v0);
+                if (state_only) {
+                    // pass 1: only the state chain, S += K~^T V per chunk
+                    ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < kC / 16; ++kk) {
+                        mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
+                               smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
+                    }
+                    mma_commit(BAR(B_SFULL));
+                    mma_commit(BAR(B_KVEMPTY0 + s));
+                    continue;
+                }
                 ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
                      mbar_wait(BAR(B_QFULL), c & 1, abort_flag, kWaitBudgetNs) &&
                      (!fact || mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs));
@@ -345,18 +396,22 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // ------------------------------------------------------------ state warpgroup
         const int r = threadIdx.x;                          // TMEM lane = dk row of S = tile row for prep
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        const int64_t hstate = ((int64_t)seq * H + h) * dk * dv;
         bool ok = true;
-        // factored form: K''_c rows = lambda^-(j+1) k_j (zero beyond the chunk), as soon as K_c lands
-        auto prep_k_fact = [&](int c) -> bool {
+        // K rows scaled as soon as K_c lands (no MMA1 reads them first): factored form K''_c rows =
+        // lambda^-(j+1) k_j; state-only pass in the direct form K~_c rows = lambda^(L-1-j) k_j.
+        // Rows beyond the chunk are zeroed.
+        const bool early_k = fact || state_only;
+        auto prep_k_early = [&](int c) -> bool {
             if (!mbar_wait(BAR(B_KVFULL0 + (c & 1)), (c >> 1) & 1, abort_flag, kWaitBudgetNs)) return false;
-            scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < chunk_len(c)) ? utab[r] : 0.f);
+            const int Lk = chunk_len(c);
+            const float f = (r < Lk) ? (fact ? utab[r] : tab[Lk - 1 - r]) : 0.f;
+            scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, f);
             fence_async_shared();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_KPREP));
             return true;
         };
-        if (fact && nchunks > 0) ok = prep_k_fact(0);
+        if (early_k && nchunks > 0) ok = prep_k_early(0);
         for (int c = 0; c <= nchunks && ok; ++c) {
             if (c >= 1) {
                 ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
@@ -378,10 +433,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
                         tmem_wait_ld();
                     } else {
-                        const float4 *src = reinterpret_cast<const float4 *>(P.h0 + hstate + (int64_t)r * dv + j0);
+                        const float4 *src = reinterpret_cast<const float4 *>(init_state + (int64_t)r * dv + j0);
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float4 x = P.h0 ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const float4 x = init_state ? __ldg(src + e) : make_float4(0.f, 0.f, 0.f, 0.f);
                             v[e >> 3][4 * (e & 7)] = __float_as_uint(x.x);
                             v[e >> 3][4 * (e & 7) + 1] = __float_as_uint(x.y);
                             v[e >> 3][4 * (e & 7) + 2] = __float_as_uint(x.z);
@@ -394,8 +449,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g_copy);
                     }
                     if (last) {
-                        if (P.hT) {
-                            float4 *dst = reinterpret_cast<float4 *>(P.hT + hstate + (int64_t)r * dv + j0);
+                        if (final_state) {
+                            float4 *dst = reinterpret_cast<float4 *>(final_state + (int64_t)r * dv + j0);
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
                                 dst[e] = make_float4(__uint_as_float(v[e >> 3][4 * (e & 7)]),
@@ -408,7 +463,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     // bf16 copy into the MN-major, 128B-swizzled S tile: one 64-column atom
                     uint8_t *atom_row = smem + o_s + (uint32_t)(j0 >> 6) * (uint32_t)dk * 128u + (uint32_t)r * 128u;
 #pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
+                    for (int q8 = 0; q8 < 8 && !state_only; ++q8) {
                         const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
                         *reinterpret_cast<uint4 *>(atom_row + (((uint32_t)q8 ^ (uint32_t)(r & 7)) << 4)) =
                             make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
@@ -435,8 +490,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SREADY));
 
-            if (fact) {
-                if (c + 1 < nchunks) ok = prep_k_fact(c + 1);
+            if (early_k) {
+                if (c + 1 < nchunks) ok = prep_k_early(c + 1);
             } else {
                 // direct form: decays of the Q and K rows, in place, once MMA1 has read them
                 ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
@@ -463,7 +518,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
         bool ok = true;
-        for (int c = 0; c < nchunks && ok; ++c) {
+        for (int c = 0; c < nchunks && ok && !state_only; ++c) {
             const int Lc = chunk_len(c);
             const int s = c & 1;
             // ---- mask: P = bf16(A .* D) ----
@@ -590,6 +645,30 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 #undef BAR
 }
 
+// Segment start states from the segments' zero-start end states (between pass 1 and pass 2):
+//   S_in(0) = h0,  S_in(s+1) = lambda^len(s) S_in(s) + E(s),
+// where every segment but the last has the same length.  One thread per 4 state elements.
+__global__ void __launch_bounds__(256)
+gla_seg_scan_kernel(const float *__restrict__ log_decay, const float *__restrict__ h0,
+                    const float *__restrict__ seg_end, float *__restrict__ seg_h0, int H, int dk, int dv,
+                    int nseg, int seg_tokens) {
+    const int chain = blockIdx.y, h = chain % H;
+    const int64_t sz = (int64_t)dk * dv;
+    const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (e >= sz) return;
+    float4 S = h0 ? __ldg(reinterpret_cast<const float4 *>(h0 + chain * sz + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float g = expf(__ldg(log_decay + h) * (float)seg_tokens);
+    for (int s = 0; s + 1 < nseg; ++s) {
+        const int64_t off = ((int64_t)chain * (nseg - 1) + s) * sz + e;
+        const float4 E = __ldg(reinterpret_cast<const float4 *>(seg_end + off));
+        S.x = fmaf(g, S.x, E.x);
+        S.y = fmaf(g, S.y, E.y);
+        S.z = fmaf(g, S.z, E.z);
+        S.w = fmaf(g, S.w, E.w);
+        *reinterpret_cast<float4 *>(seg_h0 + off) = S;
+    }
+}
+
 // ---- host side ------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -630,6 +709,37 @@ bool tc_chunk_supported(int dk, int dv, int chunk) {
     return smem_plan(dk, dv).total + 1024 <= (uint32_t)device_info().max_smem_optin;
 }
 
+namespace {
+
+// Segments per chain for a dense batch: as many as fill one wave of CTAs (one per SM), each at
+// least kMinSegChunks chunks long; 1 means the whole-chain kernel.
+constexpr int kMinSegChunks = 4;
+
+int plan_segments(int nseq, int H, int Tlen, const int32_t *cu, int *seg_chunks) {
+    const int nck = (Tlen + kC - 1) / kC;
+    *seg_chunks = nck;
+    if (cu != nullptr) return 1;
+    const long long chains = (long long)nseq * H;
+    const int sms = device_info().sm_count;
+    if (chains <= 0 || chains * 2 > sms) return 1;
+    int nseg = (int)(sms / chains);
+    nseg = nseg < nck / kMinSegChunks ? nseg : nck / kMinSegChunks;
+    if (nseg < 2) return 1;
+    *seg_chunks = (nck + nseg - 1) / nseg;
+    return (nck + *seg_chunks - 1) / *seg_chunks;
+}
+
+int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+              const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
+    if (ctas <= 0) return GLA_OK;
+    if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
+    gla_tc_chunk_kernel<<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    count_launches(1);
+    return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
+}  // namespace
+
 int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
                       float *hT, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
@@ -643,8 +753,6 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
         return GLA_ERR_LAUNCH;
     const Smem sp = smem_plan(dk, dv);
     const size_t bytes = sp.total + 1024;  // + alignment slack
-    const DeviceInfo &di = device_info();
-    if (bytes > (size_t)di.max_smem_optin) return GLA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(gla_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
         return GLA_ERR_LAUNCH;
@@ -658,11 +766,45 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.H = H;
     p.dk = dk;
     p.dv = dv;
+    p.mode = kWhole;
+    p.nseg = 1;
+    p.seg_chunks = 0;
+    p.grid_seg = 1;
+    p.seg_h0 = nullptr;
+    p.seg_end = nullptr;
     const long long chains = (long long)nseq * H;
-    if (chains > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    gla_tc_chunk_kernel<<<(unsigned)chains, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
-    count_launches(1);
-    return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
+    int seg_chunks = 0;
+    const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
+    if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, bytes, st);
+
+    // segmented schedule: stream-ordered scratch for the segment end / start states
+    const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
+    float *scratch = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), 2 * per * sizeof(float), st) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_NOMEM;
+    }
+    p.nseg = nseg;
+    p.seg_chunks = seg_chunks;
+    p.seg_end = scratch;
+    p.seg_h0 = scratch + per;
+    p.mode = kStateOnly;
+    p.grid_seg = nseg - 1;
+    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
+    if (rc == GLA_OK) {
+        dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
+        gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg,
+                                                  seg_chunks * kC);
+        count_launches(1);
+        rc = cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
+    }
+    if (rc == GLA_OK) {
+        p.mode = kSegmented;
+        p.grid_seg = nseg;
+        rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
+    }
+    cudaFreeAsync(scratch, st);
+    return rc;
 }
 
 }  // namespace gla

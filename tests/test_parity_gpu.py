@@ -126,6 +126,27 @@ def test_bf16_mild_and_strong_decays(lds):
     assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
 
 
+@pytest.mark.parametrize("B,H,T,h0_std,lds", [
+    (1, 2, 2048, 0.0, None),             # 4 segments of 4 chunks
+    (1, 3, 1000, 0.1, None),             # 2 segments, ragged last chunk
+    (2, 4, 1536, 0.05, None),            # 3 segments per chain, 8 chains
+    (1, 4, 2048, 0.1, [-0.01, -0.2, -0.5, -3.0]),  # direct decay form in both passes
+])
+def test_segmented_long_sequences(B, H, T, h0_std, lds):
+    """Few chains and many chunks: the chains are split into segments (state-only pass, scan of
+    the segment states, full pass from every segment's start state)."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=B, T=T, H=H, h0_std=h0_std)
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=12))
+    if lds is not None:
+        d["log_decay"] = torch.tensor(lds, device="cuda")
+    launches = gla.gla_kernel_launches()
+    out, hT = run_prefill(d, 128)
+    assert gla.gla_kernel_launches() - launches == 3  # pass 1, scan, pass 2
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(out.float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
+
+
 # ---- invariants on the GPU path ----
 def test_deterministic_and_causal():
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=400, H=4, h0_std=0.02)

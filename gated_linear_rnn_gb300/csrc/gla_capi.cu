@@ -22,6 +22,8 @@ int decode_step_f32(const float *, const float *, const float *, const float *, 
 bool tc_chunk_supported(int dk, int dv, int chunk);
 int tc_chunk_fwd_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *,
                       int, int, int, int, int, const int32_t *, cudaStream_t);
+int tc_chunk_fwd_bf16_noalloc(const void *, const void *, const void *, const float *, const float *, void *,
+                              float *, int, int, int, int, int, const int32_t *, cudaStream_t);
 int take_status_simt(cudaStream_t);
 int take_status_decode(cudaStream_t);
 int take_status_tc(cudaStream_t);
@@ -105,6 +107,18 @@ int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
 }
 
+int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_decay, const float *h0,
+                          void *out, float *hT, int B, int T, int H, int dk, int dv, int chunk,
+                          const int32_t *cu_seqlens, void *stream) {
+    int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+        return tc_chunk_fwd_bf16_noalloc(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens, st);
+    // the SIMT kernel takes no scratch
+    return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
+}
+
 int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *log_decay, const float *h0,
                       float *out, float *hT, int B, int T, int H, int dk, int dv, int chunk,
                       const int32_t *cu_seqlens, void *stream) {
@@ -149,6 +163,7 @@ const char *gla_status_str(int status) {
         case GLA_ERR_TIMEOUT: return "device pipeline wait timed out";
         case GLA_ERR_NOMEM: return "scratch allocation failed";
         case GLA_ERR_DEVICE_ARG: return "invalid cu_seqlens found on the device";
+        case GLA_ERR_SCRATCH_LIMIT: return "problem needs more segment-state scratch than the fixed no-alloc array";
         default: return "unknown status";
     }
 }

@@ -807,4 +807,92 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     return rc;
 }
 
+// ---- no-alloc variant ------------------------------------------------------------
+// Segment-state scratch that is part of the module image: callers of gla_chunk_fwd_noalloc
+// cannot let the library allocate, so the segmented schedule uses this array instead of
+// cudaMallocAsync.  Host code must not pass the symbol itself to a kernel (in host code it
+// is a host-side stand-in); the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) float g_noalloc_scratch[GLA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+constexpr int kMaxDev = 64;
+std::once_flag g_scratch_once[kMaxDev];
+float *g_scratch_ptr[kMaxDev];
+cudaError_t g_scratch_err[kMaxDev];
+
+// Device address of the scratch array on the current device, looked up once per device.
+float *noalloc_scratch(int *err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        *err = GLA_ERR_LAUNCH;
+        return nullptr;
+    }
+    std::call_once(g_scratch_once[dev], [dev]() {
+        void *p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        g_scratch_ptr[dev] = g_scratch_err[dev] == cudaSuccess ? static_cast<float *>(p) : nullptr;
+    });
+    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) {
+        *err = GLA_ERR_LAUNCH;
+        return nullptr;
+    }
+    *err = GLA_OK;
+    return g_scratch_ptr[dev];
+}
+}  // namespace
+
+// Same schedule as tc_chunk_fwd_bf16; only the segment-state scratch comes from the static array.
+int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const float *ld, const float *h0,
+                              void *out, float *hT, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu,
+                              cudaStream_t st) {
+    if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
+    const long long chains = (long long)nseq * H;
+    int seg_chunks = 0;
+    const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
+    if (nseg == 1) return tc_chunk_fwd_bf16(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, st);  // no scratch
+    const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
+    if (2 * per * sizeof(float) > (size_t)GLA_NOALLOC_SCRATCH_BYTES) return GLA_ERR_SCRATCH_LIMIT;
+    int err = GLA_OK;
+    float *scratch = noalloc_scratch(&err);
+    if (!scratch) return err;
+
+    const uint64_t rows = (uint64_t)nseq * (uint64_t)Tlen;
+    if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GLA_ERR_LAUNCH;
+    const size_t bytes = smem_plan(dk, dv).total + 1024;
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return GLA_ERR_LAUNCH;
+    Params p;
+    p.log_decay = ld;
+    p.h0 = h0;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.hT = hT;
+    p.cu = cu;
+    p.T = Tlen;
+    p.H = H;
+    p.dk = dk;
+    p.dv = dv;
+    p.nseg = nseg;
+    p.seg_chunks = seg_chunks;
+    p.seg_end = scratch;        // written in full by pass 1 before the scan reads it
+    p.seg_h0 = scratch + per;   // written in full by the scan before pass 2 reads it
+    p.mode = kStateOnly;
+    p.grid_seg = nseg - 1;
+    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
+    if (rc != GLA_OK) return rc;
+    dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
+    gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC);
+    count_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
+    p.mode = kSegmented;
+    p.grid_seg = nseg;
+    return launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
+}
+
 }  // namespace gla

@@ -21,12 +21,13 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgla.so")
 
 STATUS = {0: "GLA_OK", -1: "GLA_ERR_ARG", -2: "GLA_ERR_UNSUPPORTED", -3: "GLA_ERR_ALIGN", -4: "GLA_ERR_LAUNCH",
-          -5: "GLA_ERR_TIMEOUT", -6: "GLA_ERR_NOMEM", -7: "GLA_ERR_DEVICE_ARG"}
+          -5: "GLA_ERR_TIMEOUT", -6: "GLA_ERR_NOMEM", -7: "GLA_ERR_DEVICE_ARG", -8: "GLA_ERR_SCRATCH_LIMIT"}
 
 # C signatures (argtypes, restype) of every exported entry point, as declared in include/gla.h
 _P, _I = ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "gla_chunk_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_fwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_decode_step": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
@@ -132,6 +133,16 @@ def gla_chunk_fwd(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, 
     rc = load().gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
                               nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens), _stream(stream))
     _raise(rc, "gla_chunk_fwd")
+
+
+def gla_chunk_fwd_noalloc(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, stream=None) -> None:
+    """As gla_chunk_fwd, but the library allocates nothing: segment states of long sequences go to a
+    fixed scratch array in the library image (for callers that may not let a library allocate
+    device memory).  Raises GLAError(GLA_ERR_SCRATCH_LIMIT) when a problem needs more than that array."""
+    nseq, T, H, dk, dv = _chunk_args(q, k, v, log_decay, h0, out, hT, cu_seqlens, torch.bfloat16)
+    rc = load().gla_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
+                                      nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_chunk_fwd_noalloc")
 
 
 def gla_chunk_fwd_f32(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, stream=None) -> None:

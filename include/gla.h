@@ -57,7 +57,8 @@ typedef enum {
     GLA_ERR_LAUNCH = -4,       /* a CUDA call or kernel launch failed */
     GLA_ERR_TIMEOUT = -5,      /* device: a bounded pipeline wait gave up (reported by gla_last_device_status) */
     GLA_ERR_NOMEM = -6,        /* stream-ordered scratch allocation failed */
-    GLA_ERR_DEVICE_ARG = -7    /* device: cu_seqlens not non-decreasing / out of [0, T] (gla_last_device_status) */
+    GLA_ERR_DEVICE_ARG = -7,   /* device: cu_seqlens not non-decreasing / out of [0, T] (gla_last_device_status) */
+    GLA_ERR_SCRATCH_LIMIT = -8 /* gla_chunk_fwd_noalloc: the problem needs more than its fixed scratch array */
 } gla_status;
 
 /*
@@ -104,6 +105,38 @@ typedef enum {
 GLA_API int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_decay,
                   const float *h0, void *out, float *hT, int B, int T, int H, int dk, int dv,
                   int chunk, const int32_t *cu_seqlens, void *stream);
+
+/*
+ * gla_chunk_fwd_noalloc — gla_chunk_fwd for callers that may not allocate device memory.
+ *
+ * The pages describe no counterpart of this entry point; it exists for callers
+ * that cannot let a library allocate: a host whose memory manager owns the
+ * whole device pool and forbids other allocations, a serving loop with a fixed
+ * memory budget where an allocation could fail or stall at the wrong time, or a
+ * plugin host that only hands its plugins the input and output buffers.
+ *
+ * Arguments, results and errors are those of gla_chunk_fwd, computed with the
+ * same schedule.  The difference: when that schedule splits long sequences
+ * into segments, the segment states live in a scratch array that is part of
+ * the library's device image (GLA_NOALLOC_SCRATCH_BYTES bytes, reserved on
+ * every device that loads the library, until the process exits) instead of
+ * memory taken with cudaMallocAsync.  The call itself never allocates or frees
+ * device memory.  A problem whose segment states need more than that array is
+ * rejected with GLA_ERR_SCRATCH_LIMIT before anything is launched (at most
+ * 2 * min(SMs, 2 * chains) * dk * dv * 4 bytes are needed; every shape the
+ * tensor-core kernel takes fits on a GPU with up to 170 SMs).
+ *
+ * The first call on each device looks up that device's address of the array
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array and every launch overwrites the parts it reads,
+ * so nothing carries over between calls, but calls whose work overlaps on the
+ * GPU (different streams, or different host threads without ordering) race on
+ * it: serialise them.
+ */
+#define GLA_NOALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+GLA_API int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_decay,
+                                  const float *h0, void *out, float *hT, int B, int T, int H, int dk,
+                                  int dv, int chunk, const int32_t *cu_seqlens, void *stream);
 
 /* gla_chunk_fwd_f32 — as gla_chunk_fwd with f32 q, k, v and out.  Always runs
  * the SIMT kernel (f32 FMA, no tensor cores): chunk in {16, 32, 64, 128}.

@@ -281,8 +281,9 @@ def run_ours(args, world, rank, local):
         prefill()
         decode()
     torch.cuda.synchronize()
-    if gla.gla_last_device_status(stream) != 0:
-        raise SystemExit("device status after warm-up is not ok")
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after warm-up: {st_code} ({gla.gla_status_str(st_code)})")
 
     # K steps, timed as two back-to-back phases (K prefill launches, then K decode launches) so
     # neither kernel pays for the other's dirty L2 lines; every launch has its own event pair.
@@ -310,8 +311,9 @@ def run_ours(args, world, rank, local):
     pre_total = max_over_ranks(sum(pre_ms), world)
     dec_total = max_over_ranks(sum(dec_ms), world)
     step_total = max_over_ranks(sum(pre_ms) + sum(dec_ms), world)
-    if gla.gla_last_device_status(stream) != 0:
-        raise SystemExit("device status after the timed region is not ok")
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the timed region: {st_code} ({gla.gla_status_str(st_code)})")
 
     tokens = B * T * args.steps * world
     value = tokens / (pre_total / 1e3)

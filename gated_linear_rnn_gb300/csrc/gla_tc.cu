@@ -109,15 +109,19 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     p.utab = p.tab + 132 * 4;
     p.bars = p.utab + 128 * 4;
     p.bars = (p.bars + 7u) & ~7u;
-    p.slot = p.bars + 24 * 8;
+    p.slot = p.bars + 24 * 8;  // room for up to 24 barriers
     p.abort = p.slot + 4;
     p.total = p.abort + 4;
     return p;
 }
 
 // barrier indices
-enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP, B_SREADY,
+// Every barrier that can be arrived on for chunk c+1 before its waiter has passed chunk c is kept per
+// K/V stage (KPREP: the K rows of chunk c+1 may be ready before the MMA warp has waited for chunk c's);
+// with parity waits, a barrier must never run two phases ahead of a waiter.
+enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP0, B_KPREP1, B_SREADY,
        B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_OSTAGED0, B_OSTAGED1, B_FINAL, B_COUNT };
+static_assert(B_COUNT <= 24, "the shared-memory plan reserves 24 barrier slots");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -220,7 +224,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_KVEMPTY1), 1);
         mbar_init(BAR(B_AFULL), 1);
         mbar_init(BAR(B_QPREP), 4);
-        mbar_init(BAR(B_KPREP), 4);
+        mbar_init(BAR(B_KPREP0), 4);
+        mbar_init(BAR(B_KPREP1), 4);
         mbar_init(BAR(B_SREADY), 4);
         mbar_init(BAR(B_PFULL), 4);
         mbar_init(BAR(B_OFULL), 1);
@@ -328,7 +333,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (state_only) {
                     // pass 1: only the state chain, S += K~^T V per chunk
                     ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
-                         mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(B_KPREP0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
                          mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);
                     if (!ok) break;
                     tc_fence_after();
@@ -342,7 +347,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
                      mbar_wait(BAR(B_QFULL), c & 1, abort_flag, kWaitBudgetNs) &&
-                     (!fact || mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs));
+                     (!fact || mbar_wait(BAR(B_KPREP0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
                 // MMA1: A = Q K^T, K'' in the factored form (both K-major, 64B swizzle; 2 K-steps per atom)
@@ -367,7 +372,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 mma_commit(BAR(B_QEMPTY));  // Q is no longer needed: the next Q may land
                 if (!fact) {
-                    ok = mbar_wait(BAR(B_KPREP), c & 1, abort_flag, kWaitBudgetNs);
+                    ok = mbar_wait(BAR(B_KPREP0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs);
                     if (!ok) break;
                     tc_fence_after();
                 }
@@ -408,7 +413,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, f);
             fence_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_KPREP));
+            if (lane == 0) mbar_arrive(BAR(B_KPREP0 + (c & 1)));
             return true;
         };
         if (early_k && nchunks > 0) ok = prep_k_early(0);
@@ -505,7 +510,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < Lc) ? tab[Lc - 1 - r] : 0.f);
                 fence_async_shared();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(B_KPREP));
+                if (lane == 0) mbar_arrive(BAR(B_KPREP0 + (c & 1)));
             }
         }
         if (!ok) {

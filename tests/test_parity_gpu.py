@@ -161,6 +161,26 @@ def test_deterministic_and_causal():
     assert torch.equal(o1[:, :-1], o3[:, :-1])
 
 
+@pytest.mark.parametrize("name", ["layer_bf16", "long_bf16"])
+def test_repeated_launches_are_identical_and_never_time_out(name):
+    """Back-to-back launches of a full-size workload: every result bit-identical, no wait timed out
+    (a pipeline hand-off that could run a barrier two phases ahead would show up here)."""
+    w = I.WORKLOADS[name]
+    d = I.make_prefill(w, device="cuda", seed=13)
+    nseq = d["q"].shape[0]
+    outs = []
+    for it in range(40 if name == "layer_bf16" else 12):
+        out = torch.empty(d["q"].shape[:3] + (w.dv,), dtype=torch.bfloat16, device="cuda")
+        hT = torch.empty(nseq, w.H, w.dk, w.dv, dtype=torch.float32, device="cuda")
+        gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, hT, 128)
+        if it < 2:
+            outs.append((out, hT))
+    torch.cuda.synchronize()
+    assert gla.gla_last_device_status() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][0], out) and torch.equal(outs[0][1], hT)
+
+
 def test_resume_from_final_state():
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=512, H=2, h0_std=0.02)
     d = with_dev_cu(I.make_prefill(w, device="cuda", seed=8))

@@ -22,8 +22,7 @@ GLA_DEFINE_STATUS(decode)
 namespace gla {
 namespace {
 
-constexpr int kRG = 4;       // row groups per CTA
-constexpr int kUnroll = 12;  // state rows in flight per thread
+constexpr int kRG = 4;  // row groups per CTA
 
 template <typename T>
 __device__ __forceinline__ void load4(const T *p, float (&x)[4]);
@@ -41,8 +40,10 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, flo
     x[0] = fa.x; x[1] = fa.y; x[2] = fb.x; x[3] = fb.y;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(1024)
+// kMaxThreads bounds the block (and so the register budget); kUnroll state rows are in flight per
+// thread: 12 for blocks of up to 256 threads (dv <= 256), 4 for the wide blocks.
+template <typename T, int kMaxThreads, int kUnroll>
+__global__ void __launch_bounds__(kMaxThreads)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ log_decay, float *__restrict__ state, T *__restrict__ out,
               int H, int dk, int dv) {
@@ -91,8 +92,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             }
         }
     }
-    float *myred = red + rg * dv + cg * 4;
-    myred[0] = acc[0]; myred[1] = acc[1]; myred[2] = acc[2]; myred[3] = acc[3];
+    *reinterpret_cast<float4 *>(red + rg * dv + cg * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
     for (int c = tid; c < dv; c += blockDim.x) {
         float o = 0.f;
@@ -110,7 +110,10 @@ int launch_decode(const T *q, const T *k, const T *v, const float *ld, float *st
     const int threads = (dv / 4) * kRG;
     if (threads > 1024) return GLA_ERR_UNSUPPORTED;
     const size_t bytes = (size_t)(2 * dk + kRG * dv) * sizeof(float);
-    decode_kernel<T><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv);
+    if (threads <= 256)
+        decode_kernel<T, 256, 12><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv);
+    else
+        decode_kernel<T, 1024, 4><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }

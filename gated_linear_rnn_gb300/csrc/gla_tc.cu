@@ -27,13 +27,13 @@
 //              decays, the Q row decays).
 //   warps 4-7  "output" warpgroup: thread t owns TMEM lane t - 128 (a token
 //              row).  Per chunk: mask A -> P, then the output epilogue:
-//              O (TMEM) -> bf16, staged in the chunk's V tile (free once MMA2
-//              and MMA4 are done).
+//              O (TMEM) -> bf16, transposed per warp through 4 KB of shared
+//              memory so each store instruction writes four full 128-byte
+//              row segments.
 //   warp 8     TMA producer: Q (single buffer), K and V (double buffer), plus
-//              an L2 prefetch of the next chunk.
-//   warp 9     MMA issuer and TMEM owner.
-//   warp 10    TMA store of the staged O tiles; hands each K/V stage back to
-//              the producer once its store has read the tile.
+//              an L2 prefetch of the chunks ahead.
+//   warp 9     MMA issuer and TMEM owner; releases a K/V stage once MMA2 and
+//              MMA4 of its chunk are done.
 // Hand-offs are mbarriers; every wait is bounded (see sm100_ptx.cuh) and a
 // timeout is recorded as GLA_ERR_TIMEOUT in the device status word.
 //
@@ -58,10 +58,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kC = 128;              // chunk length (MMA M and the token K extent)
-constexpr int kThreads = 352;        // 8 compute warps + producer + MMA warp + store warp
+constexpr int kThreads = 320;        // 8 compute warps + producer + MMA warp
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStoreWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;        // O accumulator  [0, dv)
 constexpr uint32_t kColS = 192;      // state          [192, 192 + dv)
@@ -92,7 +91,7 @@ struct Params {
 
 // Shared memory plan (bytes from the 1024-aligned base).
 struct Smem {
-    uint32_t q, k0, k1, v0, v1, s, tab, utab, bars, slot, abort, total;
+    uint32_t q, k0, k1, v0, v1, s, xp, tab, utab, bars, slot, abort, total;
 };
 
 __host__ __device__ inline Smem smem_plan(int dk, int dv) {
@@ -105,7 +104,8 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     p.v0 = p.k1 + qk;  // MMA4 reads up to 4 atoms from a K tile: V follows, so the over-read stays in bounds
     p.v1 = p.v0 + vv;
     p.s = p.v1 + vv;
-    p.tab = p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64);
+    p.xp = p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64);  // output transpose: 4 warps x 32 rows x 128 B
+    p.tab = p.xp + 4u * 4096u;
     p.utab = p.tab + 132 * 4;
     p.bars = p.utab + 128 * 4;
     p.bars = (p.bars + 7u) & ~7u;
@@ -120,7 +120,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 // K/V stage (KPREP: the K rows of chunk c+1 may be ready before the MMA warp has waited for chunk c's);
 // with parity waits, a barrier must never run two phases ahead of a waiter.
 enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP0, B_KPREP1, B_SREADY,
-       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_OSTAGED0, B_OSTAGED1, B_FINAL, B_COUNT };
+       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_COUNT };
 static_assert(B_COUNT <= 24, "the shared-memory plan reserves 24 barrier slots");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -155,8 +155,7 @@ __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, fl
 
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const Params P) {
+                    const __grid_constant__ CUtensorMap tmV, const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int dk = P.dk, dv = P.dv, H = P.H;
@@ -164,6 +163,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // shared-memory offsets (scalars: nothing of the plan lives in local memory)
     const Smem plan = smem_plan(dk, dv);
     const uint32_t o_q = plan.q, o_k0 = plan.k0, o_k1 = plan.k1, o_v0 = plan.v0, o_v1 = plan.v1, o_s = plan.s;
+    const uint32_t o_xp = plan.xp;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + plan.bars;
 #define BAR(i) (bar0 + 8u * (uint32_t)(i))
@@ -231,8 +231,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_OFULL), 1);
         mbar_init(BAR(B_OFREE), 4);
         mbar_init(BAR(B_SFULL), 1);
-        mbar_init(BAR(B_OSTAGED0), 4);
-        mbar_init(BAR(B_OSTAGED1), 4);
         mbar_init(BAR(B_FINAL), 1);
         fence_mbar_init();
     }
@@ -286,32 +284,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     for (int a = 0; a < nva; ++a) tma_prefetch_l2_2d(&tmV, h * dv + 64 * a, yn);
                 }
             }
-            if (!ok) {
-                record_status(GLA_ERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-        }
-    } else if (warp == kStoreWarp) {
-        // ------------------------------------------------------------ output stores
-        // O of chunk c is staged (bf16, 128B swizzle) in the chunk's V tile; this warp stores it with
-        // TMA and, once the store has read the tile, hands the K/V stage back to the producer.
-        if (lane == 0 && nchunks > 0 && !state_only) {
-            tma_prefetch_desc(&tmO);
-            bool ok = true;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const int s = c & 1;
-                ok = mbar_wait(BAR(B_OSTAGED0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs);
-                if (!ok) break;
-                if (chunk_len(c) == kC) {
-                    const int y = row0 + c * kC;
-                    const uint32_t src = sbase + (s ? o_v1 : o_v0);
-                    for (int a = 0; a < nva; ++a) tma_store_2d(&tmO, h * dv + 64 * a, y, src + a * 16384u);
-                    bulk_commit();
-                    bulk_wait_read0();
-                }
-                mbar_arrive(BAR(B_KVEMPTY0 + s));
-            }
-            bulk_wait0();  // every output store has landed before the CTA exits
             if (!ok) {
                 record_status(GLA_ERR_TIMEOUT);
                 *abort_flag = 1;
@@ -391,6 +363,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_pv, 1);
                 }
                 mma_commit(BAR(B_OFULL));
+                mma_commit(BAR(B_KVEMPTY0 + s));  // MMA2 and MMA4 were the last readers of this K/V stage
             }
             if (!ok) {
                 record_status(GLA_ERR_TIMEOUT);
@@ -578,13 +551,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
 
-            // ---- output epilogue: O -> bf16 -> staged in the chunk's V tile (the store warp writes it) ----
+            // ---- output epilogue: O -> bf16, transposed per warp through shared memory so that each
+            // store instruction writes four full 128-byte row segments ----
             ok = mbar_wait(BAR(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
-            const bool full = (Lc == kC);
-            uint8_t *stage = smem + (s ? o_v1 : o_v0);  // MMA2 and MMA4 are done with this V tile
-            __nv_bfloat16 *orow = P.out + ((int64_t)(row0 + (int64_t)c * kC + r) * H + h) * dv;
+            uint8_t *xp = smem + o_xp + (uint32_t)(warp & 3) * 4096u;  // this warp's 32 rows x 128 B
+            const int wrow0 = 32 * (warp & 3);                           // first token row of this warp
             for (int j0 = 0; j0 < dv; j0 += 64) {
                 uint32_t v[2][32];
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
@@ -595,39 +568,31 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(B_OFREE));
                 }
+                // own row, 64 columns -> 128 B, 16-byte chunks swizzled by row
+                uint8_t *myrow = xp + (uint32_t)lane * 128u;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * grow);
-                    v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * grow);
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                    *reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(x[0]) * grow, __uint_as_float(x[1]) * grow),
+                        pack_bf16x2(__uint_as_float(x[2]) * grow, __uint_as_float(x[3]) * grow),
+                        pack_bf16x2(__uint_as_float(x[4]) * grow, __uint_as_float(x[5]) * grow),
+                        pack_bf16x2(__uint_as_float(x[6]) * grow, __uint_as_float(x[7]) * grow));
                 }
-                if (full) {
-                    // bf16 row into the 128B-swizzled [128 x 64] atom, the layout the O tensor map stores
-                    uint8_t *atom_row = stage + (uint32_t)(j0 >> 6) * 16384u + (uint32_t)r * 128u;
+                __syncwarp();
+                // eight lanes per row, four rows per store
 #pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
-                        *reinterpret_cast<uint4 *>(atom_row + (((uint32_t)q8 ^ (uint32_t)(r & 7)) << 4)) =
-                            make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                                       pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                                       pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                                       pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
-                    }
-                } else if (r < Lc) {
-                    // a partial chunk is followed by another sequence's rows: plain stores, row by row
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + j0);
-#pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
-                        dst[q8] = make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                                             pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                                             pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                                             pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 4 * i + (lane >> 3), ch = lane & 7;
+                    const uint4 x = *reinterpret_cast<const uint4 *>(xp + (uint32_t)rr * 128u +
+                                                                     (((uint32_t)ch ^ (uint32_t)(rr & 7)) << 4));
+                    const int row = wrow0 + rr;
+                    if (row < Lc)
+                        *reinterpret_cast<uint4 *>(P.out + ((int64_t)(row0 + (int64_t)c * kC + row) * H + h) * dv +
+                                                   j0 + 8 * ch) = x;
                 }
+                __syncwarp();
             }
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_OSTAGED0 + s));
         }
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
@@ -734,11 +699,11 @@ int plan_segments(int nseq, int H, int Tlen, const int32_t *cu, int *seg_chunks)
     return (nck + *seg_chunks - 1) / *seg_chunks;
 }
 
-int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
-              const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
+int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const Params &p, long long ctas,
+              size_t bytes, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    gla_tc_chunk_kernel<<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    gla_tc_chunk_kernel<<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, p);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -750,11 +715,10 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
     const Smem sp = smem_plan(dk, dv);
     const size_t bytes = sp.total + 1024;  // + alignment slack
@@ -780,7 +744,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     const long long chains = (long long)nseq * H;
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
-    if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, bytes, st);
+    if (nseg == 1) return launch_tc(mq, mk, mv, p, chains, bytes, st);
 
     // segmented schedule: stream-ordered scratch for the segment end / start states
     const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
@@ -795,7 +759,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.seg_h0 = scratch + per;
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mq, mk, mv, p, chains * (nseg - 1), bytes, st);
     if (rc == GLA_OK) {
         dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
         gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg,
@@ -806,7 +770,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (rc == GLA_OK) {
         p.mode = kSegmented;
         p.grid_seg = nseg;
-        rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
+        rc = launch_tc(mq, mk, mv, p, chains * nseg, bytes, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
@@ -863,11 +827,10 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
 
     const uint64_t rows = (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
     const size_t bytes = smem_plan(dk, dv).total + 1024;
     if (cudaFuncSetAttribute(gla_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
@@ -889,7 +852,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     p.seg_h0 = scratch + per;   // written in full by the scan before pass 2 reads it
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mq, mk, mv, p, chains * (nseg - 1), bytes, st);
     if (rc != GLA_OK) return rc;
     dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
     gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC);
@@ -897,7 +860,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     p.mode = kSegmented;
     p.grid_seg = nseg;
-    return launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
+    return launch_tc(mq, mk, mv, p, chains * nseg, bytes, st);
 }
 
 }  // namespace gla

@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/gla.h"
+#include "gla.h"
 
 namespace gla {
 

@@ -30,8 +30,7 @@
 //              O (TMEM) -> bf16, transposed per warp through 4 KB of shared
 //              memory so each store instruction writes four full 128-byte
 //              row segments.
-//   warp 8     TMA producer: Q (single buffer), K and V (double buffer), plus
-//              an L2 prefetch of the chunks ahead.
+//   warp 8     TMA producer: Q (single buffer), K and V (double buffer).
 //   warp 9     MMA issuer and TMEM owner; releases a K/V stage once MMA2 and
 //              MMA4 of its chunk are done.
 // Hand-offs are mbarriers; every wait is bounded (see sm100_ptx.cuh) and a
@@ -66,7 +65,6 @@ constexpr uint32_t kColO = 0;        // O accumulator  [0, dv)
 constexpr uint32_t kColS = 192;      // state          [192, 192 + dv)
 constexpr uint32_t kColA = 384;      // A = Q K^T      [384, 512); P aliases [384, 448)
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;  // 4 s per wait
-constexpr int kL2Ahead = 2;          // chunks of L2 prefetch ahead of the current load
 
 // Launch modes.  A long dense sequence with few (sequence, head) chains is cut into nseg
 // segments of seg_chunks chunks: pass 1 (kStateOnly) computes every segment's end state from a zero
@@ -271,17 +269,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     mbar_expect_tx(BAR(B_QFULL), qbytes);
                     for (int a = 0; a < nka; ++a)
                         tma_load_2d(sbase + o_q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_QFULL));
-                }
-                // Warm L2 two chunks ahead: the shared-memory stages only allow loads one chunk
-                // ahead, which is shorter than the HBM latency under load, so the loads that do
-                // go out should find their lines already in L2.
-                for (int cp = (c == 0 ? 1 : c + kL2Ahead); cp <= c + kL2Ahead && cp < nchunks; ++cp) {
-                    const int yn = row0 + cp * kC;
-                    for (int a = 0; a < nka; ++a) {
-                        if (!state_only) tma_prefetch_l2_2d(&tmQ, h * dk + 32 * a, yn);
-                        tma_prefetch_l2_2d(&tmK, h * dk + 32 * a, yn);
-                    }
-                    for (int a = 0; a < nva; ++a) tma_prefetch_l2_2d(&tmV, h * dv + 64 * a, yn);
                 }
             }
             if (!ok) {

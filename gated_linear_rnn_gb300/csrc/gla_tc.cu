@@ -19,17 +19,21 @@
 // The state rows are dk (<= 128), padded to M = 128; rows >= dk of the state
 // accumulator are never read.
 //
-// Warp roles (320 threads):
+// Warp roles (448 threads):
 //   warps 0-3  "state" warpgroup: thread t owns TMEM lane t (a dk row of S).
 //              Per chunk: state pass (read the state accumulator from TMEM,
 //              finish S_{c-1}, write its bf16 copy for MMA3 and the f32 value
 //              back for MMA4), then the K row decays in place (and, for strong
 //              decays, the Q row decays).
-//   warps 4-7  "output" warpgroup: thread t owns TMEM lane t - 128 (a token
-//              row).  Per chunk: mask A -> P, then the output epilogue:
-//              O (TMEM) -> bf16, transposed per warp through 4 KB of shared
-//              memory so each store instruction writes four full 128-byte
-//              row segments.
+//   warps 4-7  "mask" warpgroup: thread t owns TMEM lane t - 128 (a token row).
+//              Per chunk: mask A -> P.
+//   warps 10-13 "epilogue" warpgroup (TMEM lane quadrant = warp % 4): O (TMEM)
+//              -> bf16, 64 columns at a time, into a 4 KB staging tile per
+//              warp laid out as a 128B-swizzled TMA box, then one TMA store
+//              per tile; a tile is refilled once its previous store has read
+//              it.  O leaves TMEM at the pace of the TMEM loads, so MMA3 of
+//              the next chunk is not held up by global stores.  The mask of
+//              chunk c+1 and the epilogue of chunk c overlap.
 //   warp 8     TMA producer: Q (single buffer), K and V (double buffer).
 //   warp 9     MMA issuer and TMEM owner; releases a K/V stage once MMA2 and
 //              MMA4 of its chunk are done.
@@ -57,7 +61,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kC = 128;              // chunk length (MMA M and the token K extent)
-constexpr int kThreads = 320;        // 8 compute warps + producer + MMA warp
+constexpr int kThreads = 448;        // state, mask and epilogue warpgroups + producer + MMA warp
+constexpr int kEpiWarp0 = 10;        // first warp of the epilogue warpgroup
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -102,7 +107,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     p.v0 = p.k1 + qk;  // MMA4 reads up to 4 atoms from a K tile: V follows, so the over-read stays in bounds
     p.v1 = p.v0 + vv;
     p.s = p.v1 + vv;
-    p.xp = p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64);  // output transpose: 4 warps x 32 rows x 128 B
+    p.xp = p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64);  // output staging: 4 warps x 32 rows x 128 B
     p.tab = p.xp + 4u * 4096u;
     p.utab = p.tab + 132 * 4;
     p.bars = p.utab + 128 * 4;
@@ -153,7 +158,8 @@ __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, fl
 
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const Params P) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int dk = P.dk, dv = P.dv, H = P.H;
@@ -251,6 +257,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
+            if (!state_only) tma_prefetch_desc(&tmO);
             const uint32_t kvbytes = (uint32_t)nka * 8192u + (uint32_t)nva * 16384u;
             const uint32_t qbytes = (uint32_t)nka * 8192u;
             bool ok = true;
@@ -478,14 +485,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             *abort_flag = 1;
         }
     } else if (warp < 8) {
-        // ------------------------------------------------------------ output warpgroup
+        // ------------------------------------------------------------ mask warpgroup
         const int r = threadIdx.x - 128;                    // TMEM lane = token row
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
         bool ok = true;
         for (int c = 0; c < nchunks && ok && !state_only; ++c) {
             const int Lc = chunk_len(c);
-            const int s = c & 1;
             // ---- mask: P = bf16(A .* D) ----
             ok = mbar_wait(BAR(B_AFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
@@ -510,19 +515,18 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         }
                     } else {
                         // D_rj = lambda^(r-j): walk j downwards from 32b+31, one factor of lambda per step
-                        float dec[32];
                         const int dtop = r - (32 * b + 31);
                         float f = tab[max(dtop, 0)];
 #pragma unroll
-                        for (int e = 31; e >= 0; --e) {
-                            const bool on = row_ok && (dtop + (31 - e) >= 0);
-                            dec[e] = on ? f : 0.f;
-                            f = on ? f * lam : f;
+                        for (int e = 15; e >= 0; --e) {
+                            const bool on1 = row_ok && (dtop + (30 - 2 * e) >= 0);
+                            const float d1 = on1 ? f : 0.f;
+                            f = on1 ? f * lam : f;
+                            const bool on0 = row_ok && (dtop + (31 - 2 * e) >= 0);
+                            const float d0 = on0 ? f : 0.f;
+                            f = on0 ? f * lam : f;
+                            p[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * d0, __uint_as_float(a[2 * e + 1]) * d1);
                         }
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            p[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * dec[2 * e],
-                                               __uint_as_float(a[2 * e + 1]) * dec[2 * e + 1]);
                     }
                     asm volatile(
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -538,13 +542,29 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_PFULL));
 
-            // ---- output epilogue: O -> bf16, transposed per warp through shared memory so that each
-            // store instruction writes four full 128-byte row segments ----
+        }
+        if (!ok) {
+            record_status(GLA_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------------------ epilogue warpgroup
+        const int q4 = warp & 3;                            // TMEM lane quadrant of this warp
+        const int r = 32 * q4 + lane;                       // TMEM lane = token row
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
+        uint8_t *xp = smem + o_xp + (uint32_t)q4 * 4096u;     // this warp's staging tile: 32 rows x 128 B
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok && !state_only; ++c) {
+            const int Lc = chunk_len(c);
+            // ---- output epilogue: O -> bf16 rows in this warp's 4 KB staging tile (one 64-column
+            // group of its 32 rows, laid out as a 128B-swizzled TMA box), then a TMA store per group.
+            // Only the staging tile's previous store must have read it before it is refilled, so O
+            // leaves TMEM at the pace of the TMEM loads, not of the global stores. ----
             ok = mbar_wait(BAR(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
-            uint8_t *xp = smem + o_xp + (uint32_t)(warp & 3) * 4096u;  // this warp's 32 rows x 128 B
-            const int wrow0 = 32 * (warp & 3);                           // first token row of this warp
+            const bool full = (Lc == kC);
             for (int j0 = 0; j0 < dv; j0 += 64) {
                 uint32_t v[2][32];
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
@@ -555,7 +575,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     __syncwarp();
                     if (lane == 0) mbar_arrive(BAR(B_OFREE));
                 }
-                // own row, 64 columns -> 128 B, 16-byte chunks swizzled by row
+                if (lane == 0) bulk_wait_read0();  // the previous store out of the staging tile has read it
+                __syncwarp();
+                // own row (lane): 64 columns -> 128 B, 16-byte chunk q8 at q8 ^ (lane & 7)
                 uint8_t *myrow = xp + (uint32_t)lane * 128u;
 #pragma unroll
                 for (int q8 = 0; q8 < 8; ++q8) {
@@ -566,27 +588,39 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         pack_bf16x2(__uint_as_float(x[4]) * grow, __uint_as_float(x[5]) * grow),
                         pack_bf16x2(__uint_as_float(x[6]) * grow, __uint_as_float(x[7]) * grow));
                 }
-                __syncwarp();
-                // eight lanes per row, four rows per store
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = 4 * i + (lane >> 3), ch = lane & 7;
-                    const uint4 x = *reinterpret_cast<const uint4 *>(xp + (uint32_t)rr * 128u +
-                                                                     (((uint32_t)ch ^ (uint32_t)(rr & 7)) << 4));
-                    const int row = wrow0 + rr;
-                    if (row < Lc)
-                        *reinterpret_cast<uint4 *>(P.out + ((int64_t)(row0 + (int64_t)c * kC + row) * H + h) * dv +
-                                                   j0 + 8 * ch) = x;
+                if (full) {
+                    fence_async_shared();  // the staged rows must be visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmO, h * dv + j0, row0 + c * kC + 32 * q4, sbase + o_xp + (uint32_t)q4 * 4096u);
+                        bulk_commit();
+                    }
+                } else {
+                    // partial chunk: the rows from Lc on belong to the next sequence or lie past the
+                    // tensor, so the rows below Lc are stored with plain predicated stores, eight lanes
+                    // per row
+                    __syncwarp();
+                    const int ch = lane & 7;
+#pragma unroll 4
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3), row = 32 * q4 + rr;
+                        if (row < Lc) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(
+                                xp + (uint32_t)rr * 128u + (((uint32_t)ch ^ (uint32_t)(rr & 7)) << 4));
+                            *reinterpret_cast<uint4 *>(P.out + ((row0 + (int64_t)c * kC + row) * H + h) * dv + j0 +
+                                                       8 * ch) = x;
+                        }
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
+        if (lane == 0) bulk_wait_read0();  // no store may still read shared memory at exit
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
             *abort_flag = 1;
         }
     }
-
     // ---- teardown: all roles done; make sure no tensor-core work is in flight, free TMEM ----
     tc_fence_before();
     __syncthreads();
@@ -646,12 +680,12 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              CUtensorMapSwizzle sw) {
+              CUtensorMapSwizzle sw, uint32_t box_rows = kC) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {box_cols, (cuuint32_t)kC};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -686,11 +720,11 @@ int plan_segments(int nseq, int H, int Tlen, const int32_t *cu, int *seg_chunks)
     return (nck + *seg_chunks - 1) / *seg_chunks;
 }
 
-int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const Params &p, long long ctas,
-              size_t bytes, cudaStream_t st) {
+int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+              const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    gla_tc_chunk_kernel<<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, p);
+    gla_tc_chunk_kernel<<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -702,10 +736,11 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
         return GLA_ERR_LAUNCH;
     const Smem sp = smem_plan(dk, dv);
     const size_t bytes = sp.total + 1024;  // + alignment slack
@@ -731,7 +766,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     const long long chains = (long long)nseq * H;
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
-    if (nseg == 1) return launch_tc(mq, mk, mv, p, chains, bytes, st);
+    if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, bytes, st);
 
     // segmented schedule: stream-ordered scratch for the segment end / start states
     const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
@@ -746,7 +781,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.seg_h0 = scratch + per;
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mq, mk, mv, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
     if (rc == GLA_OK) {
         dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
         gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg,
@@ -757,7 +792,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (rc == GLA_OK) {
         p.mode = kSegmented;
         p.grid_seg = nseg;
-        rc = launch_tc(mq, mk, mv, p, chains * nseg, bytes, st);
+        rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
@@ -814,10 +849,11 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
 
     const uint64_t rows = (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
         return GLA_ERR_LAUNCH;
     const size_t bytes = smem_plan(dk, dv).total + 1024;
     if (cudaFuncSetAttribute(gla_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
@@ -839,7 +875,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     p.seg_h0 = scratch + per;   // written in full by the scan before pass 2 reads it
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mq, mk, mv, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
     if (rc != GLA_OK) return rc;
     dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
     gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC);
@@ -847,7 +883,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     p.mode = kSegmented;
     p.grid_seg = nseg;
-    return launch_tc(mq, mk, mv, p, chains * nseg, bytes, st);
+    return launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
 }
 
 }  // namespace gla

@@ -61,6 +61,8 @@ def _load():
             lib.gla_oracle_chunked.restype = I
             lib.gla_oracle_decode_step.argtypes = [P, P, P, P, P, P, I, I, I, I, I]
             lib.gla_oracle_decode_step.restype = I
+            lib.gla_oracle_backward.argtypes = [P] * 13 + [I, I, I, I, P, I, I]
+            lib.gla_oracle_backward.restype = I
             _lib = lib
     return _lib
 
@@ -155,6 +157,34 @@ def quadratic(q, k, v, log_decay, h0=None, cu_seqlens=None, units=None, nthreads
 def chunked(q, k, v, log_decay, chunk, h0=None, cu_seqlens=None, units=None, nthreads=None):
     """Chunkwise form with chunk length ``chunk`` ([L3B] §挑战 1, Figure 3), fp64."""
     return _run("chunked", q, k, v, log_decay, h0, cu_seqlens, units, chunk=chunk, nthreads=nthreads)
+
+
+def backward(q, k, v, dout, log_decay, h0=None, dhT=None, cu_seqlens=None, units=None, nthreads=None):
+    """Gradients of L = sum(dout * o) + sum(dhT * hT) through the recurrence ([L3B] §挑战 3).
+
+    Reverse-mode chain rule of S_t = lam S_{t-1} + k_t^T v_t, o_t = q_t S_t, one token at a
+    time (see ``gla_oracle.c``).  dout has the shape of o; dhT (optional) that of hT.  Returns
+    (dq, dk, dv, dh0) in float64 with the shapes of q, k, v and h0 ([nseq, H, dk, dv])."""
+    q, k, v, ld, h0, starts, lens, nseq, (B, T, H, dk, dv) = _prepare(q, k, v, log_decay, h0, cu_seqlens)
+    do = _f32(dout)
+    if do.shape != (B, T, H, dv):
+        raise ValueError("dout must have the shape of o")
+    if dhT is not None:
+        dhT = _f64(dhT)
+        if dhT.shape != (nseq, H, dk, dv):
+            raise ValueError(f"dhT must be {(nseq, H, dk, dv)}")
+    dq = np.zeros((B, T, H, dk), dtype=np.float64)
+    dkk = np.zeros((B, T, H, dk), dtype=np.float64)
+    dvv = np.zeros((B, T, H, dv), dtype=np.float64)
+    dh0 = np.zeros((nseq, H, dk, dv), dtype=np.float64)
+    u, nu = _units_arr(units)
+    nt = default_threads() if nthreads is None else int(nthreads)
+    rc = _load().gla_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(ld), _ptr(h0), _ptr(dhT),
+                                     _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dh0), _ptr(starts), _ptr(lens),
+                                     nseq, H, dk, dv, _ptr(u), nu, nt)
+    if rc != 0:
+        raise ValueError("oracle backward rejected its arguments")
+    return dq, dkk, dvv, dh0
 
 
 def decode_step(q, k, v, log_decay, state, nthreads=None):

@@ -312,3 +312,148 @@ int gla_oracle_decode_step(const float *q, const float *k, const float *v, const
     for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
     return 0;
 }
+
+/*
+ * Backward (vector-Jacobian product) of the recurrence, for training.
+ * [L3B] §"挑战 3" (the backward pass differentiates every sequential state
+ * update of the recurrence); the page prints no backward formulas, so this is
+ * the chain rule applied to the [L3B] GLA-mixer recurrence, one token at a
+ * time, in reverse:
+ *   given dO = dL/do_t and dhT = dL/dS_T (NULL = 0), with G = dL/dS_t,
+ *   G_T = dhT;  for t = T .. 1:
+ *       G     += q_t^T do_t                 (o_t = q_t S_t)
+ *       dq_t   = do_t S_t^T
+ *       dk_t   = v_t G^T,   dv_t = k_t G    (S_t = lam S_{t-1} + k_t^T v_t)
+ *       G      = lam G                      (gradient reaching S_{t-1})
+ *   dh0 = G.
+ * The forward states S_t are replayed from checkpoints kept every kCkpt
+ * tokens (the replay repeats the forward's own operations, so the replayed
+ * states equal the stored ones bit for bit).
+ *   do  : [rows, H, dv] float32;   dhT, dh0 : [nseq, H, dk, dv] float64
+ *   dq, dk : [rows, H, dk] float64; dv : [rows, H, dv] float64
+ */
+typedef struct {
+    const float *q, *k, *v, *dout;
+    const double *log_decay, *h0, *dhT;
+    double *dq, *dk, *dv, *dh0;
+    const int64_t *seq_start, *seq_len;
+    int nseq, H, dk_, dv_;
+    const int32_t *units;
+    int nunits, next_unit, error;
+} bwd_t;
+
+enum { kCkpt = 64 };
+
+/* one forward token step on S (dk x dv): S = lam S + k^T v */
+static void state_step(double *S, const float *kt, const float *vt, double lam, int dk, int dv) {
+    for (int i = 0; i < dk; ++i)
+        for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] = lam * S[(size_t)i * dv + j] + (double)kt[i] * (double)vt[j];
+}
+
+static int chain_backward(const bwd_t *J, int s, int h) {
+    const int H = J->H, dk = J->dk_, dv = J->dv_;
+    const size_t sz = (size_t)dk * dv;
+    const double lam = exp(J->log_decay[h]);
+    const int64_t T = J->seq_len[s], r0 = J->seq_start[s];
+    const int64_t nck = (T + kCkpt - 1) / kCkpt;
+    double *ck = (double *)calloc((size_t)(nck > 0 ? nck : 1) * sz, sizeof(double)); /* S before block b */
+    double *blk = (double *)malloc((size_t)kCkpt * sz * sizeof(double));             /* S_t inside a block */
+    double *G = (double *)calloc(sz, sizeof(double));
+    double *S = (double *)calloc(sz, sizeof(double));
+    if (!ck || !blk || !G || !S) { free(ck); free(blk); free(G); free(S); return -1; }
+    /* forward sweep: checkpoints of S_{b*kCkpt} (state before the block's first token) */
+    if (J->h0) memcpy(S, J->h0 + ((size_t)s * H + h) * sz, sizeof(double) * sz);
+    for (int64_t t = 0; t < T; ++t) {
+        if (t % kCkpt == 0) memcpy(ck + (size_t)(t / kCkpt) * sz, S, sizeof(double) * sz);
+        const int64_t row = r0 + t;
+        state_step(S, J->k + ((size_t)row * H + h) * dk, J->v + ((size_t)row * H + h) * dv, lam, dk, dv);
+    }
+    free(S);
+    if (J->dhT) memcpy(G, J->dhT + ((size_t)s * H + h) * sz, sizeof(double) * sz);
+    /* reverse sweep, one block at a time (last block first) */
+    for (int64_t b = nck - 1; b >= 0; --b) {
+        const int64_t t0 = b * kCkpt, t1 = (t0 + kCkpt < T) ? t0 + kCkpt : T;
+        /* replay the block: blk[u] = S_{t0+u} after the update at token t0+u */
+        const double *prev = ck + (size_t)b * sz;
+        for (int64_t t = t0; t < t1; ++t) {
+            double *cur = blk + (size_t)(t - t0) * sz;
+            memcpy(cur, prev, sizeof(double) * sz);
+            const int64_t row = r0 + t;
+            state_step(cur, J->k + ((size_t)row * H + h) * dk, J->v + ((size_t)row * H + h) * dv, lam, dk, dv);
+            prev = cur;
+        }
+        for (int64_t t = t1 - 1; t >= t0; --t) {
+            const int64_t row = r0 + t;
+            const float *qt = J->q + ((size_t)row * H + h) * dk;
+            const float *kt = J->k + ((size_t)row * H + h) * dk;
+            const float *vt = J->v + ((size_t)row * H + h) * dv;
+            const float *dot = J->dout + ((size_t)row * H + h) * dv;
+            const double *St = blk + (size_t)(t - t0) * sz;
+            double *dqt = J->dq + ((size_t)row * H + h) * dk;
+            double *dkt = J->dk + ((size_t)row * H + h) * dk;
+            double *dvt = J->dv + ((size_t)row * H + h) * dv;
+            for (int i = 0; i < dk; ++i)               /* G += q_t^T do_t */
+                for (int j = 0; j < dv; ++j) G[(size_t)i * dv + j] += (double)qt[i] * (double)dot[j];
+            for (int i = 0; i < dk; ++i) {             /* dq_t = do_t S_t^T;  dk_t = v_t G^T */
+                double aq = 0.0, ak = 0.0;
+                for (int j = 0; j < dv; ++j) {
+                    aq += (double)dot[j] * St[(size_t)i * dv + j];
+                    ak += (double)vt[j] * G[(size_t)i * dv + j];
+                }
+                dqt[i] = aq;
+                dkt[i] = ak;
+            }
+            for (int j = 0; j < dv; ++j) {             /* dv_t = k_t G */
+                double a = 0.0;
+                for (int i = 0; i < dk; ++i) a += (double)kt[i] * G[(size_t)i * dv + j];
+                dvt[j] = a;
+            }
+            for (size_t e = 0; e < sz; ++e) G[e] *= lam;   /* to S_{t-1} */
+        }
+    }
+    if (J->dh0) memcpy(J->dh0 + ((size_t)s * H + h) * sz, G, sizeof(double) * sz);
+    free(ck);
+    free(blk);
+    free(G);
+    return 0;
+}
+
+static void *bwd_worker(void *arg) {
+    bwd_t *J = (bwd_t *)arg;
+    const int total = J->units ? J->nunits : J->nseq * J->H;
+    for (;;) {
+        const int u = __atomic_fetch_add(&J->next_unit, 1, __ATOMIC_RELAXED);
+        if (u >= total) break;
+        int s, h;
+        if (J->units) { s = J->units[2 * u]; h = J->units[2 * u + 1]; }
+        else { s = u / J->H; h = u % J->H; }
+        if (s < 0 || s >= J->nseq || h < 0 || h >= J->H) { J->error = 1; continue; }
+        if (chain_backward(J, s, h) != 0) J->error = 1;
+    }
+    return NULL;
+}
+
+int gla_oracle_backward(const float *q, const float *k, const float *v, const float *dout,
+                        const double *log_decay, const double *h0, const double *dhT, double *dq,
+                        double *dk, double *dv, double *dh0, const int64_t *seq_start,
+                        const int64_t *seq_len, int nseq, int H, int dk_, int dv_,
+                        const int32_t *units, int nunits, int nthreads) {
+    if (!q || !k || !v || !dout || !log_decay || !dq || !dk || !dv || !seq_start || !seq_len) return -1;
+    if (nseq < 0 || H <= 0 || dk_ <= 0 || dv_ <= 0) return -1;
+    for (int s = 0; s < nseq; ++s)
+        if (seq_len[s] < 0 || seq_start[s] < 0) return -1;
+    bwd_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v; J.dout = dout; J.log_decay = log_decay; J.h0 = h0; J.dhT = dhT;
+    J.dq = dq; J.dk = dk; J.dv = dv; J.dh0 = dh0; J.seq_start = seq_start; J.seq_len = seq_len;
+    J.nseq = nseq; J.H = H; J.dk_ = dk_; J.dv_ = dv_; J.units = units; J.nunits = nunits;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    pthread_t tid[512];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&tid[started], NULL, bwd_worker, &J) == 0) ++started;
+    bwd_worker(&J);
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    return J.error ? -1 : 0;
+}

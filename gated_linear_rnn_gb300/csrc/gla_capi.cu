@@ -24,6 +24,12 @@ int tc_chunk_fwd_bf16(const void *, const void *, const void *, const float *, c
                       int, int, int, int, int, const int32_t *, cudaStream_t);
 int tc_chunk_fwd_bf16_noalloc(const void *, const void *, const void *, const float *, const float *, void *,
                               float *, int, int, int, int, int, const int32_t *, cudaStream_t);
+int simt_chunk_bwd_f32(const float *, const float *, const float *, const float *, const float *, const float *,
+                       const float *, float *, float *, float *, float *, int, int, int, int, int, int,
+                       const int32_t *, cudaStream_t);
+int simt_chunk_bwd_bf16(const void *, const void *, const void *, const void *, const float *, const float *,
+                        const float *, void *, void *, void *, float *, int, int, int, int, int, int,
+                        const int32_t *, cudaStream_t);
 int take_status_simt(cudaStream_t);
 int take_status_decode(cudaStream_t);
 int take_status_tc(cudaStream_t);
@@ -73,6 +79,17 @@ int check_prefill(const void *q, const void *k, const void *v, const float *ld, 
         !aligned16(hT) || !aligned16(ld) || !aligned16(cu))
         return GLA_ERR_ALIGN;
     if (!device_info().ok) return GLA_ERR_UNSUPPORTED;
+    return GLA_OK;
+}
+
+int check_backward(const void *q, const void *k, const void *v, const void *dout, const float *ld,
+                   const float *h0, const float *dhT, const void *dq, const void *dk, const void *dv,
+                   const float *dh0, int B, int T, int H, int dkk, int dvv, const int32_t *cu) {
+    if (!dout || !dq || !dk || !dv) return GLA_ERR_ARG;
+    int rc = check_prefill(q, k, v, ld, h0, dout, nullptr, B, T, H, dkk, dvv, cu);
+    if (rc) return rc;
+    if (!aligned16(dhT) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dh0))
+        return GLA_ERR_ALIGN;
     return GLA_OK;
 }
 
@@ -128,6 +145,24 @@ int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, const floa
                               (cudaStream_t)stream);
 }
 
+int gla_chunk_bwd(const void *q, const void *k, const void *v, const void *dout, const float *log_decay,
+                  const float *h0, const float *dhT, void *dq, void *dk_out, void *dv_out, float *dh0, int B, int T,
+                  int H, int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream) {
+    int rc = check_backward(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    return simt_chunk_bwd_bf16(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, chunk,
+                               cu_seqlens, (cudaStream_t)stream);
+}
+
+int gla_chunk_bwd_f32(const float *q, const float *k, const float *v, const float *dout, const float *log_decay,
+                      const float *h0, const float *dhT, float *dq, float *dk_out, float *dv_out, float *dh0, int B,
+                      int T, int H, int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream) {
+    int rc = check_backward(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    return simt_chunk_bwd_f32(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, chunk,
+                              cu_seqlens, (cudaStream_t)stream);
+}
+
 int gla_decode_step(const void *q, const void *k, const void *v, const float *log_decay, float *state_inout,
                     void *out, int N, int H, int dk, int dv, void *stream) {
     int rc = check_decode(q, k, v, log_decay, state_inout, out, N, H, dk, dv);
@@ -170,6 +205,6 @@ const char *gla_status_str(int status) {
 
 uint64_t gla_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int gla_version(void) { return 100; }
+int gla_version(void) { return 200; }
 
 }  // extern "C"

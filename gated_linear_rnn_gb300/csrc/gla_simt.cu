@@ -13,6 +13,18 @@
 //   A   = (Q K^T) .* D,          D_ij = lambda^(i-j) for j <= i else 0
 //   O   = A V + diag(lambda^(i+1)) Q S
 //   S   = lambda^L S + K^T diag(lambda^(L-1-j)) V
+//
+// The same kernel runs the three recurrences of the backward pass (the page's
+// section "挑战 3": the backward differentiates every sequential state update).
+// With G_t = dL/dS_t, G_t = lambda G_{t+1} + q_t^T do_t and G_T = dhT, the
+// gradients are dq_t = do_t S_t^T, dk_t = v_t G_t^T, dv_t = k_t G_t and
+// dh0 = lambda G_1.  Each is a GLA-type recurrence with roles exchanged:
+//   dv: reversed time, q' = k, k' = q, v' = do, initial state dhT
+//   dk: reversed time, q' = v, k' = do, v' = q, initial state dhT^T
+//   dq: forward time,  q' = do, k' = v, v' = k, initial state h0^T
+// so the kernel takes a time direction, an initial state read transposed, an
+// initial state that enters without the first step's decay (G_T = dhT is not
+// decayed before q_T^T do_T is added) and a final state scaled by lambda.
 #include <algorithm>
 
 #include "gla_common.cuh"
@@ -44,12 +56,19 @@ __host__ __device__ inline SimtSmem simt_layout(int C, int dk, int dvt) {
     return L;
 }
 
-template <typename T, int C>
+// Initial / final state handling for the backward's recurrences (all zero for the forward).
+enum : int {
+    kH0Transposed = 1,  // h0 is stored [dv][dk] per chain: S[d][c] = h0[c][d]
+    kH0Undecayed = 2,   // h0 enters the first step without its decay: S_1 = h0 + k_1^T v_1
+    kHTTimesDecay = 4,  // hT is written as lambda * S_T
+};
+
+template <typename T, int C, bool Rev>
 __global__ void __launch_bounds__(kThreads)
 simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                   const float *__restrict__ log_decay, const float *__restrict__ h0,
                   T *__restrict__ out, float *__restrict__ hT, int nseq, int Tlen, int H, int dk,
-                  int dv, int dvt, const int32_t *__restrict__ cu) {
+                  int dv, int dvt, const int32_t *__restrict__ cu, int state_mode) {
     extern __shared__ float smem[];
     const SimtSmem Lo = simt_layout(C, dk, dvt);
     float *Qs = smem + Lo.q, *Ks = smem + Lo.k, *Vs = smem + Lo.vv, *As = smem + Lo.a;
@@ -74,20 +93,29 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
 
     // state tile: S[d][c] for c < dvt (columns beyond nc kept at zero)
     const size_t sbase = ((size_t)s * H + h) * dk * dv;
+    const bool h0t = (state_mode & kH0Transposed) != 0;
     for (int e = tid; e < dk * dvt; e += kThreads) {
         const int d = e / dvt, c = e % dvt;
-        Ss[e] = (h0 != nullptr && c < nc) ? __ldg(h0 + sbase + (size_t)d * dv + j0 + c) : 0.f;
+        const size_t off = h0t ? (size_t)(j0 + c) * dk + d : (size_t)d * dv + j0 + c;
+        Ss[e] = (h0 != nullptr && c < nc) ? __ldg(h0 + sbase + off) : 0.f;
     }
+    // token row of chunk-local position i in the chunk that starts c0 tokens into the walk
+    auto row_of = [&](int64_t c0, int i) -> int64_t {
+        return Rev ? r.start + r.len - 1 - (c0 + i) : r.start + c0 + i;
+    };
 
     for (int64_t c0 = 0; c0 < r.len; c0 += C) {
         const int L = (r.len - c0 < (int64_t)C) ? (int)(r.len - c0) : C;
+        // decay exponents of the carried-state terms are one lower in the first chunk when the
+        // initial state enters undecayed
+        const int sh = (c0 == 0 && (state_mode & kH0Undecayed)) ? 1 : 0;
         __syncthreads();
         // ---- load the chunk (rows >= L are zero) ----
         for (int e = tid; e < C * dk; e += kThreads) {
             const int i = e / dk, d = e % dk;
             float qv = 0.f, kv = 0.f;
             if (i < L) {
-                const size_t off = ((size_t)(r.start + c0 + i) * H + h) * dk + d;
+                const size_t off = ((size_t)row_of(c0, i) * H + h) * dk + d;
                 qv = to_f32(q[off]);
                 kv = to_f32(k[off]);
             }
@@ -97,7 +125,7 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         for (int e = tid; e < C * dvt; e += kThreads) {
             const int i = e / dvt, c = e % dvt;
             float vv = 0.f;
-            if (i < L && c < nc) vv = to_f32(v[((size_t)(r.start + c0 + i) * H + h) * dv + j0 + c]);
+            if (i < L && c < nc) vv = to_f32(v[((size_t)row_of(c0, i) * H + h) * dv + j0 + c]);
             Vs[i * dvtp + c] = vv;
         }
         __syncthreads();
@@ -158,8 +186,8 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
             for (int a = 0; a < 4; ++a) {
                 const int i = bi * 4 + a;
                 if (i >= L) continue;
-                const float g = tab[i + 1];
-                T *orow = out + ((size_t)(r.start + c0 + i) * H + h) * dv + j0;
+                const float g = tab[i + 1 - sh];
+                T *orow = out + ((size_t)row_of(c0, i) * H + h) * dv + j0;
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     const int c = bc * 4 + b;
@@ -169,7 +197,7 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
         }
         __syncthreads();
         // ---- S = lambda^L S + K^T diag(lambda^(L-1-j)) V ----
-        const float gL = tab[L];
+        const float gL = tab[L - sh];
         for (int blk = tid; blk < (dk / 4) * (dvt / 4); blk += kThreads) {
             const int bd = blk / (dvt / 4), bc = blk % (dvt / 4);
             float acc[4][4] = {};
@@ -196,16 +224,18 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     }
     __syncthreads();
     if (hT != nullptr) {
+        // dh0 = lambda G_1; an empty sequence has no step, so its dh0 is dhT itself
+        const float gT = ((state_mode & kHTTimesDecay) && r.len > 0) ? tab[1] : 1.f;
         for (int e = tid; e < dk * dvt; e += kThreads) {
             const int d = e / dvt, c = e % dvt;
-            if (c < nc) hT[sbase + (size_t)d * dv + j0 + c] = Ss[e];
+            if (c < nc) hT[sbase + (size_t)d * dv + j0 + c] = gT * Ss[e];
         }
     }
 }
 
-template <typename T, int C>
+template <typename T, int C, bool Rev>
 int launch_c(const T *q, const T *k, const T *v, const float *ld, const float *h0, T *out, float *hT,
-             int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
+             int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, int state_mode, cudaStream_t st) {
     const DeviceInfo &di = device_info();
     const size_t limit = std::min<size_t>((size_t)di.max_smem_optin, 200 * 1024);
     int dvt = 64;
@@ -217,31 +247,32 @@ int launch_c(const T *q, const T *k, const T *v, const float *ld, const float *h
         bytes = simt_layout(C, dk, dvt).total * sizeof(float);
     }
     if (bytes > limit) return GLA_ERR_UNSUPPORTED;
-    auto kern = simt_chunk_kernel<T, C>;
+    auto kern = simt_chunk_kernel<T, C, Rev>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
         return GLA_ERR_LAUNCH;
     const long long chains = (long long)nseq * H;
     const int tiles = (dv + dvt - 1) / dvt;
     if (chains > 0x7fffffffLL || tiles > 65535) return GLA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)chains, (unsigned)tiles);
-    kern<<<grid, kThreads, bytes, st>>>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, dvt, cu);
+    kern<<<grid, kThreads, bytes, st>>>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, dvt, cu, state_mode);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
 
-template <typename T>
+template <typename T, bool Rev = false>
 int launch_simt(const T *q, const T *k, const T *v, const float *ld, const float *h0, T *out, float *hT,
-                int nseq, int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st) {
+                int nseq, int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st,
+                int state_mode = 0) {
     if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return GLA_ERR_UNSUPPORTED;
     // A chunk whose tiles do not fit in shared memory is processed as sub-chunks
     // of half the length (the chunked form is the same map for any chunk length).
     int rc = GLA_ERR_UNSUPPORTED;
     for (int c = chunk; c >= 16 && rc == GLA_ERR_UNSUPPORTED; c /= 2) {
         switch (c) {
-            case 16: rc = launch_c<T, 16>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, st); break;
-            case 32: rc = launch_c<T, 32>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, st); break;
-            case 64: rc = launch_c<T, 64>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, st); break;
-            default: rc = launch_c<T, 128>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, st); break;
+            case 16: rc = launch_c<T, 16, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
+            case 32: rc = launch_c<T, 32, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
+            case 64: rc = launch_c<T, 64, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
+            default: rc = launch_c<T, 128, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
         }
     }
     return rc;
@@ -261,6 +292,37 @@ int simt_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float
     using B = __nv_bfloat16;
     return launch_simt<B>((const B *)q, (const B *)k, (const B *)v, ld, h0, (B *)out, hT, nseq, Tlen, H, dk,
                           dv, chunk, cu, st);
+}
+
+// Backward of the chunked forward: three recurrences (see the top of this file), each a launch of
+// the chunk kernel.  dq, dk: [rows, H, dk]; dv: [rows, H, dv]; dh0: [nseq, H, dk, dv] or null;
+// dhT: [nseq, H, dk, dv] or null (zero); h0 as in the forward.
+template <typename T>
+int simt_bwd(const T *q, const T *k, const T *v, const T *dout, const float *ld, const float *h0, const float *dhT,
+             T *dq, T *dk_, T *dv_, float *dh0, int nseq, int Tlen, int H, int dk, int dv, int chunk,
+             const int32_t *cu, cudaStream_t st) {
+    int rc = launch_simt<T, true>(k, q, dout, ld, dhT, dv_, dh0, nseq, Tlen, H, dk, dv, chunk, cu, st,
+                                  kH0Undecayed | kHTTimesDecay);
+    if (rc != GLA_OK) return rc;
+    rc = launch_simt<T, true>(v, dout, q, ld, dhT, dk_, nullptr, nseq, Tlen, H, dv, dk, chunk, cu, st,
+                              kH0Undecayed | kH0Transposed);
+    if (rc != GLA_OK) return rc;
+    return launch_simt<T, false>(dout, v, k, ld, h0, dq, nullptr, nseq, Tlen, H, dv, dk, chunk, cu, st,
+                                 kH0Transposed);
+}
+
+int simt_chunk_bwd_f32(const float *q, const float *k, const float *v, const float *dout, const float *ld,
+                       const float *h0, const float *dhT, float *dq, float *dk_, float *dv_, float *dh0, int nseq,
+                       int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st) {
+    return simt_bwd<float>(q, k, v, dout, ld, h0, dhT, dq, dk_, dv_, dh0, nseq, Tlen, H, dk, dv, chunk, cu, st);
+}
+
+int simt_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *dout, const float *ld,
+                        const float *h0, const float *dhT, void *dq, void *dk_, void *dv_, float *dh0, int nseq,
+                        int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st) {
+    using B = __nv_bfloat16;
+    return simt_bwd<B>((const B *)q, (const B *)k, (const B *)v, (const B *)dout, ld, h0, dhT, (B *)dq, (B *)dk_,
+                       (B *)dv_, dh0, nseq, Tlen, H, dk, dv, chunk, cu, st);
 }
 
 }  // namespace gla

@@ -29,6 +29,8 @@ SIGNATURES = {
     "gla_chunk_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_fwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_bwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_decode_step": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_last_device_status": ([_P], _I),
@@ -153,6 +155,36 @@ def gla_chunk_fwd_f32(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=No
     _raise(rc, "gla_chunk_fwd_f32")
 
 
+def _bwd_args(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, cu_seqlens, dtype):
+    nseq, T, H, dk_, dv_ = _chunk_args(q, k, v, log_decay, h0, dout, dhT, cu_seqlens, dtype)
+    B = q.shape[0]
+    _check(dq, "dq", dtype, (B, T, H, dk_))
+    _check(dk, "dk", dtype, (B, T, H, dk_))
+    _check(dv, "dv", dtype, (B, T, H, dv_))
+    _check(dh0, "dh0", torch.float32, (nseq, H, dk_, dv_), allow_none=True)
+    return nseq, T, H, dk_, dv_
+
+
+def gla_chunk_bwd(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, chunk: int, cu_seqlens=None,
+                  stream=None) -> None:
+    """bf16 backward of the chunked forward: writes dq, dk, dv and (if given) dh0.  See include/gla.h."""
+    nseq, T, H, dk_, dv_ = _bwd_args(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, cu_seqlens, torch.bfloat16)
+    rc = load().gla_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(log_decay), _ptr(h0), _ptr(dhT),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), nseq, T, H, dk_, dv_, int(chunk),
+                              _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_chunk_bwd")
+
+
+def gla_chunk_bwd_f32(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, chunk: int, cu_seqlens=None,
+                      stream=None) -> None:
+    """f32 backward of the chunked forward (SIMT kernel).  See include/gla.h."""
+    nseq, T, H, dk_, dv_ = _bwd_args(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, cu_seqlens, torch.float32)
+    rc = load().gla_chunk_bwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(log_decay), _ptr(h0), _ptr(dhT),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), nseq, T, H, dk_, dv_, int(chunk),
+                                  _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_chunk_bwd_f32")
+
+
 def _decode_args(q, k, v, log_decay, state, out, dtype):
     if q.dim() != 3:
         raise ValueError("q must be [N, H, dk]")
@@ -214,6 +246,17 @@ def chunk_fwd(q, k, v, log_decay, h0=None, chunk: int = 128, cu_seqlens=None, fi
     else:
         gla_chunk_fwd(q, k, v, log_decay, h0, out, hT, chunk, cu_seqlens, stream)
     return out, hT
+
+
+def chunk_bwd(q, k, v, dout, log_decay, h0=None, dhT=None, chunk: int = 128, cu_seqlens=None, stream=None):
+    """Allocate and return (dq, dk, dv, dh0) for the chunked forward's gradients."""
+    nseq = q.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+    dq, dk = torch.empty_like(q), torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dh0 = torch.empty((nseq, q.shape[2], q.shape[3], v.shape[-1]), dtype=torch.float32, device=q.device)
+    fn = gla_chunk_bwd_f32 if q.dtype == torch.float32 else gla_chunk_bwd
+    fn(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, chunk, cu_seqlens, stream)
+    return dq, dk, dv, dh0
 
 
 def decode_step(q, k, v, log_decay, state, stream=None):

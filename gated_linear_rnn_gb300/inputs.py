@@ -139,6 +139,20 @@ def make_prefill(w: Workload, device="cpu", seed: int = 0, lengths=None, T: Opti
     return {"q": q, "k": k, "v": v, "log_decay": ld, "h0": h0, "cu_seqlens": cu, "chunk": w.chunk}
 
 
+def make_backward(w: Workload, device="cpu", seed: int = 0, lengths=None, T: Optional[int] = None,
+                  B: Optional[int] = None, dhT_std: float = 0.02):
+    """Inputs for the backward of a prefill workload: make_prefill's tensors for ``seed``, plus
+    dout ~ N(0, 1) with the shape of the output (``w.dtype``) and dhT ~ N(0, dhT_std^2) fp32
+    (None when dhT_std is 0), drawn in that order from a generator seeded with seed + 1000003."""
+    d = make_prefill(w, device=device, seed=seed, lengths=lengths, T=T, B=B)
+    dev = torch.device(device)
+    g = _gen(dev, seed + 1000003)
+    nseq = d["q"].shape[0] if d["cu_seqlens"] is None else d["cu_seqlens"].numel() - 1
+    d["dout"] = _randn(tuple(d["q"].shape[:3]) + (w.dv,), g, dev).to(w.torch_dtype)
+    d["dhT"] = _randn((nseq, w.H, w.dk, w.dv), g, dev, dhT_std) if dhT_std > 0 else None
+    return d
+
+
 def make_decode(w: Workload, device="cpu", seed: int = 0, N: Optional[int] = None):
     """Inputs for one decode step: q, k [N,H,dk], v [N,H,dv] (``w.dtype``), state fp32."""
     dev = torch.device(device)

@@ -147,6 +147,42 @@ GLA_API int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, co
                       int chunk, const int32_t *cu_seqlens, void *stream);
 
 /*
+ * gla_chunk_bwd — gradients of the chunked forward, for training (page
+ * "线性注意力模型如何实现固定推理状态", section "挑战 3": the backward pass
+ * differentiates every sequential state update; the page prints no formulas,
+ * so these are the chain rule of the recurrence).  With
+ *     L = sum(dout .* out) + sum(dhT .* hT),   G_t = dL/dS_t:
+ *     G_T = dhT + q_T^T do_T,   G_t = lambda_h G_{t+1} + q_t^T do_t
+ *     dq_t = do_t S_t^T,   dk_t = v_t G_t^T,   dv_t = k_t G_t,   dh0 = lambda_h G_1
+ * (S_t the forward states).  Each of dv, dk and dq is a chunked recurrence of
+ * the same form as the forward: dv and dk walk each sequence backwards in time
+ * (from the state dhT), dq forwards (from h0); three launches in all.
+ *
+ *   q, k         [B, T, H, dk] bf16 (packed [1, T, H, dk] with cu_seqlens)
+ *   v, dout      [B, T, H, dv] bf16
+ *   log_decay    [H] f32
+ *   h0           [B|N, H, dk, dv] f32 or NULL (zeros), as in the forward
+ *   dhT          [B|N, H, dk, dv] f32 or NULL (zeros): gradient with respect to hT
+ *   dq, dk       [B, T, H, dk] bf16, written
+ *   dv           [B, T, H, dv] bf16, written
+ *   dh0          [B|N, H, dk, dv] f32, written; NULL to skip
+ *   B, T, H, dk, dv, chunk, cu_seqlens, stream: as gla_chunk_fwd
+ * Runs on the SIMT kernel (f32 accumulation): chunk in {16, 32, 64, 128};
+ * chunks whose tiles do not fit in shared memory run as shorter sub-chunks.
+ * No pointer may alias another.  Returns a gla_status; no scratch is taken.
+ */
+GLA_API int gla_chunk_bwd(const void *q, const void *k, const void *v, const void *dout, const float *log_decay,
+                          const float *h0, const float *dhT, void *dq, void *dk_out, void *dv_out, float *dh0,
+                          int B, int T, int H, int dk, int dv, int chunk, const int32_t *cu_seqlens,
+                          void *stream);
+
+/* gla_chunk_bwd_f32 — as gla_chunk_bwd with f32 q, k, v, dout, dq, dk_out, dv_out. */
+GLA_API int gla_chunk_bwd_f32(const float *q, const float *k, const float *v, const float *dout,
+                              const float *log_decay, const float *h0, const float *dhT, float *dq,
+                              float *dk_out, float *dv_out, float *dh0, int B, int T, int H, int dk, int dv,
+                              int chunk, const int32_t *cu_seqlens, void *stream);
+
+/*
  * gla_decode_step — one recurrent decode step for N independent sequences
  * (page "线性注意力模型如何实现固定推理状态", section "i14 与 Laplace 3B 架构":
  * O(1) work per generated token with a fixed-size state; section "Trainium2 上的

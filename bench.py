@@ -57,6 +57,22 @@ def prefill_flops(B, T, H, dk, dv, C):
     return B * T * H * (2 * C * (dk + dv) + 4 * dk * dv)
 
 
+def backward_flops(B, T, H, dk, dv, C):
+    """f32 FMA work of gla_chunk_bwd per launch: three chunked recurrences (dv: dk x dv state,
+    dk and dq: dv x dk state), each C(dk'+dv')/2 x 2 causal intra FLOPs (the SIMT kernel skips the
+    masked half) plus 2 dk dv for the carried-state term and 2 dk dv for the state update per
+    token-head.  The dk and dq passes run as sub-chunks of min(C, 64) tokens (their dk' = dv tiles)."""
+    per = lambda c, a, b: c * (a + b) + 4 * a * b  # noqa: E731
+    c2 = min(C, 64) if dv > 128 else C
+    return B * T * H * (per(C, dk, dv) + 2 * per(c2, dv, dk))
+
+
+def backward_bytes(B, T, H, dk, dv):
+    """HBM bytes of gla_chunk_bwd per launch (bf16): each of its three passes reads three token
+    tensors and writes one (dv: k, q, dout -> dv; dk: v, dout, q -> dk; dq: dout, v, k -> dq)."""
+    return B * T * H * 2 * ((dk + dk + dv + dv) + (dv + dv + dk + dk) + (dv + dv + dk + dk))
+
+
 def decode_bytes(N, H, dk, dv):
     state = N * H * dk * dv * 4 * 2
     io = N * H * (2 * dk + 2 * dv) * 2
@@ -329,6 +345,9 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the public API: pinned host inputs in, results back to the host ----
     e2e = run_e2e(args, P, D, w, wd, out, hT, dout, stream)
 
+    # ---- backward of the layer prefill (training path), timed on its own after the step ----
+    bwd = run_backward(args, P, w, stream, peaks, peak_src) if args.bwd_steps > 0 else None
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_total / args.steps, "higher_is_better": True,
@@ -350,6 +369,7 @@ def run_ours(args, world, rank, local):
                    "us_per_step": dec_avg_s * 1e6, "state_bytes": sbytes, "io_bytes": iobytes,
                    "tokens_per_s": wd.B * world / dec_avg_s},
         "e2e": e2e,
+        "backward": bwd,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
@@ -361,6 +381,59 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_backward(args, P, w, stream, peaks, peak_src):
+    """gla_chunk_bwd on the layer workload (h0 = 0, dhT = 0, dout ~ N(0, 1)); CUDA events per launch."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    g = torch.Generator(device=P["q"].device).manual_seed(1000003)
+    do = torch.randn(P["v"].shape, generator=g, device=P["q"].device).to(torch.bfloat16)
+    dq, dk_, dv_ = (torch.empty_like(P[k]) for k in ("q", "k", "v"))
+    dh0 = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=P["q"].device)
+
+    def step():
+        gla.gla_chunk_bwd(P["q"], P["k"], P["v"], do, P["log_decay"], None, None, dq, dk_, dv_, dh0, w.chunk,
+                          None, stream)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.bwd_steps)]
+    for e in ev:
+        e[0].record(stream)
+        step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the backward: {st_code} ({gla.gla_status_str(st_code)})")
+    ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    fl = backward_flops(w.B, w.T, w.H, w.dk, w.dv, w.chunk)
+    by = backward_bytes(w.B, w.T, w.H, w.dk, w.dv)
+    alu_peak = fp32_fma_peak_tflops()
+    tfl = fl / (ms / 1e3) / 1e12
+    return {"value": w.B * w.T / (ms / 1e3), "unit": "tokens/s", "ms": ms, "launches_per_call": 3,
+            "steps": args.bwd_steps,
+            "roofline": {"bound": "alu", "achieved": tfl, "peak": alu_peak, "unit": "TFLOP/s", "frac": tfl / alu_peak,
+                         "peak_source": "derived: SMs x 128 f32 FMA lanes x 2 FLOP x max SM clock",
+                         "flops_per_launch": fl},
+            "hbm_gbs": by / (ms / 1e3) / 1e9, "bytes_per_launch": by,
+            "kernel": "gla_chunk_bwd (layer_bf16, SIMT f32 FMA, three recurrences)"}
+
+
+def fp32_fma_peak_tflops():
+    """f32 FMA peak from unit counts and clocks: 128 FP32 lanes per SM, 2 FLOP per FMA, max SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = 2070.0
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits",
+                              f"--id={torch.cuda.current_device()}"], capture_output=True, text=True, timeout=10)
+        mhz = float(out.stdout.strip().splitlines()[0])
+    except Exception:
+        pass
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
 
 
 def run_e2e(args, P, D, w, wd, out, hT, dout, stream):
@@ -421,6 +494,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-steps", type=int, default=5, help="timed launches of the backward (0: skip)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of fp64 reference work to time")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -61,3 +61,11 @@ def test_algorithmic_counts():
     assert bench.prefill_flops(1, 1, 1, 96, 192, 128) == 147456
     state, io = bench.decode_bytes(1280, 16, 96, 192)
     assert state == 1280 * 16 * 96 * 192 * 8 and io == 1280 * 16 * 576 * 2
+
+
+def test_backward_counts():
+    import bench
+    # three passes, each three token tensors read and one written: 3 x 1,152 B per token-head (bf16)
+    assert bench.backward_bytes(1, 1, 1, 96, 192) == 3 * 1152
+    # dv pass at C = 128 (dk x dv state), dk and dq passes as 64-token sub-chunks (dv x dk state)
+    assert bench.backward_flops(1, 1, 1, 96, 192, 128) == (128 * 288 + 4 * 96 * 192) + 2 * (64 * 288 + 4 * 96 * 192)

@@ -345,6 +345,9 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the public API: pinned host inputs in, results back to the host ----
     e2e = run_e2e(args, P, D, w, wd, out, hT, dout, stream)
 
+    # ---- paged decode: the same step through a slot table (a permutation of the state pages) ----
+    paged = run_paged_decode(args, D, wd, dout, stream, peaks)
+
     # ---- backward of the layer prefill (training path), timed on its own after the step ----
     bwd = run_backward(args, P, w, stream, peaks, peak_src) if args.bwd_steps > 0 else None
 
@@ -369,6 +372,7 @@ def run_ours(args, world, rank, local):
                    "us_per_step": dec_avg_s * 1e6, "state_bytes": sbytes, "io_bytes": iobytes,
                    "tokens_per_s": wd.B * world / dec_avg_s},
         "e2e": e2e,
+        "decode_paged": paged,
         "backward": bwd,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -381,6 +385,37 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_paged_decode(args, D, wd, dout, stream, peaks):
+    """gla_decode_step_paged over the decode workload's states as a pool, rows in a seeded random
+    page order; CUDA events per launch, median."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    g = torch.Generator().manual_seed(7)
+    slots = torch.randperm(wd.B, generator=g).to(torch.int32).to(D["q"].device)
+
+    def step():
+        gla.gla_decode_step_paged(D["q"], D["k"], D["v"], D["log_decay"], D["state"], slots, dout, stream)
+
+    for _ in range(3):
+        step()
+    n = max(3, min(args.steps, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for e in ev:
+        e[0].record(stream)
+        step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the paged decode: {st_code} ({gla.gla_status_str(st_code)})")
+    us = statistics.median(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    sbytes, iobytes = decode_bytes(wd.B, wd.H, wd.dk, wd.dv)
+    iobytes += wd.B * 4  # the slot table
+    return {"us_per_step": us, "unit": "state GB/s", "value": sbytes / (us / 1e6) / 1e9,
+            "frac_of_hbm_peak": (sbytes + iobytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"], "steps": n,
+            "rows": wd.B, "pool_pages": wd.B}
 
 
 def run_backward(args, P, w, stream, peaks, peak_src):

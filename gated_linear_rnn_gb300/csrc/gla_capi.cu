@@ -19,6 +19,8 @@ int decode_step_bf16(const void *, const void *, const void *, const float *, fl
                      int, cudaStream_t);
 int decode_step_f32(const float *, const float *, const float *, const float *, float *, float *, int, int,
                     int, int, cudaStream_t);
+int decode_step_paged_bf16(const void *, const void *, const void *, const float *, float *, const int32_t *, int,
+                           void *, int, int, int, int, cudaStream_t);
 bool tc_chunk_supported(int dk, int dv, int chunk);
 int tc_chunk_fwd_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *,
                       int, int, int, int, int, const int32_t *, cudaStream_t);
@@ -175,6 +177,17 @@ int gla_decode_step_f32(const float *q, const float *k, const float *v, const fl
     int rc = check_decode(q, k, v, log_decay, state_inout, out, N, H, dk, dv);
     if (rc) return rc;
     return decode_step_f32(q, k, v, log_decay, state_inout, out, N, H, dk, dv, (cudaStream_t)stream);
+}
+
+int gla_decode_step_paged(const void *q, const void *k, const void *v, const float *log_decay, float *state_pool,
+                          const int32_t *slots, int nslots, void *out, int N, int H, int dk, int dv, void *stream) {
+    if (!slots || nslots <= 0) return GLA_ERR_ARG;
+    int rc = check_decode(q, k, v, log_decay, state_pool, out, N, H, dk, dv);
+    if (rc) return rc;
+    if (!aligned16(slots)) return GLA_ERR_ALIGN;
+    if ((long long)nslots * H > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
+    return decode_step_paged_bf16(q, k, v, log_decay, state_pool, slots, nslots, out, N, H, dk, dv,
+                                  (cudaStream_t)stream);
 }
 
 int gla_last_device_status(void *stream) {

@@ -15,6 +15,14 @@
 // covers 512 contiguous bytes of a row), issuing UNROLL loads before using any
 // of them so that enough bytes are in flight per SM.  The read-out sum over dk
 // is finished through shared memory across the row groups.
+//
+// Paged form (same section: the serving engine gives every sequence one fixed
+// state page in its pool, and every new batch width was a separate compiled
+// shape, so batches were padded to a fixed width): the state of batch row n is
+// page slots[n] of a pool of nslots pages; a negative slot marks a padding row,
+// whose output is zero and which touches no page.  The kernel is the same for
+// every width, and a fixed-width padded call can be captured in a CUDA graph
+// and replayed with new slot tables.
 #include "gla_common.cuh"
 
 GLA_DEFINE_STATUS(decode)
@@ -46,7 +54,7 @@ template <typename T, int kMaxThreads, int kUnroll>
 __global__ void __launch_bounds__(kMaxThreads)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ log_decay, float *__restrict__ state, T *__restrict__ out,
-              int H, int dk, int dv) {
+              int H, int dk, int dv, const int32_t *__restrict__ slots, int nslots) {
     extern __shared__ float sm[];
     float *qs = sm, *ks = sm + dk, *red = sm + 2 * dk;  // red: [kRG][dv]
     const int unit = blockIdx.x;                          // n * H + h
@@ -54,6 +62,17 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const int ncg = dv >> 2;
     const int tid = threadIdx.x;
     const int cg = tid % ncg, rg = tid / ncg;
+    size_t page = (size_t)unit;  // state page of this (n, h): unit itself unless paged
+    if (slots != nullptr) {
+        const int n = unit / H;
+        const int slot = __ldg(slots + n);
+        if (slot < 0 || slot >= nslots) {  // padding row (or a bad slot, reported): zero output, no page
+            if (slot >= nslots && tid == 0) record_status(GLA_ERR_DEVICE_ARG);
+            for (int c = tid; c < dv; c += blockDim.x) out[(size_t)unit * dv + c] = from_f32<T>(0.f);
+            return;
+        }
+        page = (size_t)slot * H + h;
+    }
 
     for (int i = tid; i < dk; i += blockDim.x) {
         qs[i] = to_f32(q[(size_t)unit * dk + i]);
@@ -64,7 +83,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const float lam = expf(__ldg(log_decay + h));
     __syncthreads();
 
-    float4 *S = reinterpret_cast<float4 *>(state + (size_t)unit * dk * dv) + cg;
+    float4 *S = reinterpret_cast<float4 *>(state + page * dk * dv) + cg;
     const int row_f4 = ncg;  // float4 per state row
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int r0 = rg; r0 < dk; r0 += kRG * kUnroll) {
@@ -104,16 +123,18 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 
 template <typename T>
 int launch_decode(const T *q, const T *k, const T *v, const float *ld, float *state, T *out, int N, int H,
-                  int dk, int dv, cudaStream_t st) {
+                  int dk, int dv, cudaStream_t st, const int32_t *slots = nullptr, int nslots = 0) {
     const long long units = (long long)N * H;
     if (units > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     const int threads = (dv / 4) * kRG;
     if (threads > 1024) return GLA_ERR_UNSUPPORTED;
     const size_t bytes = (size_t)(2 * dk + kRG * dv) * sizeof(float);
     if (threads <= 256)
-        decode_kernel<T, 256, 12><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv);
+        decode_kernel<T, 256, 12><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv,
+                                                                           slots, nslots);
     else
-        decode_kernel<T, 1024, 4><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv);
+        decode_kernel<T, 1024, 4><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv,
+                                                                           slots, nslots);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -129,6 +150,14 @@ int decode_step_bf16(const void *q, const void *k, const void *v, const float *l
 int decode_step_f32(const float *q, const float *k, const float *v, const float *ld, float *state, float *out,
                     int N, int H, int dk, int dv, cudaStream_t st) {
     return launch_decode<float>(q, k, v, ld, state, out, N, H, dk, dv, st);
+}
+
+int decode_step_paged_bf16(const void *q, const void *k, const void *v, const float *ld, float *pool,
+                           const int32_t *slots, int nslots, void *out, int N, int H, int dk, int dv,
+                           cudaStream_t st) {
+    using B = __nv_bfloat16;
+    return launch_decode<B>((const B *)q, (const B *)k, (const B *)v, ld, pool, (B *)out, N, H, dk, dv, st, slots,
+                            nslots);
 }
 
 }  // namespace gla

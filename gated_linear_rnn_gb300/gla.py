@@ -33,6 +33,7 @@ SIGNATURES = {
     "gla_chunk_bwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_decode_step": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "gla_decode_step_paged": ([_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "gla_last_device_status": ([_P], _I),
     "gla_status_str": ([_I], ctypes.c_char_p),
     "gla_kernel_launches": ([], ctypes.c_uint64),
@@ -212,6 +213,24 @@ def gla_decode_step_f32(q, k, v, log_decay, state_inout, out, stream=None) -> No
     rc = load().gla_decode_step_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(state_inout), _ptr(out),
                                     N, H, dk, dv, _stream(stream))
     _raise(rc, "gla_decode_step_f32")
+
+
+def gla_decode_step_paged(q, k, v, log_decay, state_pool, slots, out, stream=None) -> None:
+    """bf16 decode step on a page pool: row n updates page slots[n] (negative: padding row, zero out)."""
+    if q.dim() != 3 or state_pool.dim() != 4:
+        raise ValueError("q must be [N, H, dk] and state_pool [nslots, H, dk, dv]")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (N, H, dk))
+    _check(v, "v", torch.bfloat16, (N, H, dv))
+    _check(out, "out", torch.bfloat16, (N, H, dv))
+    _check(log_decay, "log_decay", torch.float32, (H,))
+    _check(state_pool, "state_pool", torch.float32, (state_pool.shape[0], H, dk, dv))
+    _check(slots, "slots", torch.int32, (N,))
+    rc = load().gla_decode_step_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(state_pool), _ptr(slots),
+                                      int(state_pool.shape[0]), _ptr(out), N, H, dk, dv, _stream(stream))
+    _raise(rc, "gla_decode_step_paged")
 
 
 def gla_last_device_status(stream=None) -> int:

@@ -207,6 +207,31 @@ GLA_API int gla_decode_step_f32(const float *q, const float *k, const float *v, 
                         float *state_inout, float *out, int N, int H, int dk, int dv, void *stream);
 
 /*
+ * gla_decode_step_paged — gla_decode_step with the states kept in a pool of
+ * fixed pages, one page per sequence (page "线性注意力模型如何实现固定推理状态",
+ * section "Trainium2 上的推理优化": the serving engine hands every sequence a
+ * fixed state page in its pool; each new decode batch width cost a separate
+ * compiled shape, so batches were padded to fixed widths).  Row n of the batch
+ * uses page slots[n]:
+ *     S = state_pool[slots[n]]:  S <- lambda_h S + k^T v;  out[n] = q S
+ * A negative slot marks a padding row: its out row is written as zeros and no
+ * page is touched.  Any N runs with the same kernel; a padded fixed-width call
+ * makes no allocation or host synchronisation, so it can be captured in a
+ * CUDA graph and replayed after rewriting `slots` (and q, k, v) in place.
+ *
+ *   q, k, v, out, log_decay, N, H, dk, dv: as gla_decode_step (bf16)
+ *   state_pool   [nslots, H, dk, dv] f32, pages read and written in place
+ *   slots        [N] int32 on the device; each slot < nslots or negative
+ *   nslots       pages in the pool (> 0)
+ * Two rows must not name the same page (their updates would race).  A slot
+ * >= nslots is a device-side error: the row is treated as padding and
+ * GLA_ERR_DEVICE_ARG is recorded for gla_last_device_status.
+ */
+GLA_API int gla_decode_step_paged(const void *q, const void *k, const void *v, const float *log_decay,
+                                  float *state_pool, const int32_t *slots, int nslots, void *out, int N, int H,
+                                  int dk, int dv, void *stream);
+
+/*
  * gla_last_device_status — synchronise `stream`, then return and clear the
  * device status word: GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_DEVICE_ARG for the
  * first failure recorded by any kernel of this library on the current device

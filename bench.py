@@ -58,19 +58,19 @@ def prefill_flops(B, T, H, dk, dv, C):
 
 
 def backward_flops(B, T, H, dk, dv, C):
-    """f32 FMA work of gla_chunk_bwd per launch: three chunked recurrences (dv: dk x dv state,
-    dk and dq: dv x dk state), each C(dk'+dv')/2 x 2 causal intra FLOPs (the SIMT kernel skips the
-    masked half) plus 2 dk dv for the carried-state term and 2 dk dv for the state update per
-    token-head.  The dk and dq passes run as sub-chunks of min(C, 64) tokens (their dk' = dv tiles)."""
-    per = lambda c, a, b: c * (a + b) + 4 * a * b  # noqa: E731
-    c2 = min(C, 64) if dv > 128 else C
-    return B * T * H * (per(C, dk, dv) + 2 * per(c2, dv, dk))
+    """Tensor-core FLOPs issued per gla_chunk_bwd launch as full tiles (chunk C = 128): two state
+    passes (M = 128 over dk, N = dv, K = C per chunk) and, per chunk, the scores K Q^T, V dO^T,
+    dO V^T and dV = P dO + K G, dK = P Q + V G^T, dQ = P K + dO S^T.  Per token-head:
+    2 x 2 x 128 x dv + 6 C (dk + dv) + 6 dk dv."""
+    return B * T * H * (4 * 128 * dv + 6 * C * (dk + dv) + 6 * dk * dv)
 
 
-def backward_bytes(B, T, H, dk, dv):
-    """HBM bytes of gla_chunk_bwd per launch (bf16): each of its three passes reads three token
-    tensors and writes one (dv: k, q, dout -> dv; dk: v, dout, q -> dk; dq: dout, v, k -> dq)."""
-    return B * T * H * 2 * ((dk + dk + dv + dv) + (dv + dv + dk + dk) + (dv + dv + dk + dk))
+def backward_bytes(B, T, H, dk, dv, C=128):
+    """Algorithmic HBM bytes per gla_chunk_bwd launch (bf16 tensors, bf16 state tiles): the state
+    passes read k, v and q, dout; the gradient kernel reads q, k, v, dout and writes dq, dk, dv;
+    the two bf16 state tiles per chunk are written once and read once."""
+    per_token_head = 2 * 2 * (dk + dv) + 2 * 2 * (dk + dv) + 2 * (2 * dk + dv) + 8 * dk * dv // C
+    return B * T * H * per_token_head
 
 
 def decode_bytes(N, H, dk, dv):
@@ -419,7 +419,7 @@ def run_paged_decode(args, D, wd, dout, stream, peaks):
 
 
 def run_backward(args, P, w, stream, peaks, peak_src):
-    """gla_chunk_bwd on the layer workload (h0 = 0, dhT = 0, dout ~ N(0, 1)); CUDA events per launch."""
+    """gla_chunk_bwd on the layer workload (h0 = 0, dhT = 0, dout ~ N(0, 1)); CUDA events per call."""
     import torch
     from gated_linear_rnn_gb300 import gla
     g = torch.Generator(device=P["q"].device).manual_seed(1000003)
@@ -431,44 +431,33 @@ def run_backward(args, P, w, stream, peaks, peak_src):
         gla.gla_chunk_bwd(P["q"], P["k"], P["v"], do, P["log_decay"], None, None, dq, dk_, dv_, dh0, w.chunk,
                           None, stream)
 
-    for _ in range(2):
+    for _ in range(3):
         step()
     torch.cuda.synchronize()
+    l0 = gla.gla_kernel_launches()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.bwd_steps)]
     for e in ev:
         e[0].record(stream)
         step()
         e[1].record(stream)
     torch.cuda.synchronize()
+    launches = (gla.gla_kernel_launches() - l0) // max(1, args.bwd_steps)
     st_code = gla.gla_last_device_status(stream)
     if st_code != 0:
         raise SystemExit(f"device status after the backward: {st_code} ({gla.gla_status_str(st_code)})")
     ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     fl = backward_flops(w.B, w.T, w.H, w.dk, w.dv, w.chunk)
-    by = backward_bytes(w.B, w.T, w.H, w.dk, w.dv)
-    alu_peak = fp32_fma_peak_tflops()
+    by = backward_bytes(w.B, w.T, w.H, w.dk, w.dv, w.chunk)
+    gbs = by / (ms / 1e3) / 1e9
     tfl = fl / (ms / 1e3) / 1e12
-    return {"value": w.B * w.T / (ms / 1e3), "unit": "tokens/s", "ms": ms, "launches_per_call": 3,
+    return {"value": w.B * w.T / (ms / 1e3), "unit": "tokens/s", "ms": ms, "launches_per_call": launches,
             "steps": args.bwd_steps,
-            "roofline": {"bound": "alu", "achieved": tfl, "peak": alu_peak, "unit": "TFLOP/s", "frac": tfl / alu_peak,
-                         "peak_source": "derived: SMs x 128 f32 FMA lanes x 2 FLOP x max SM clock",
-                         "flops_per_launch": fl},
-            "hbm_gbs": by / (ms / 1e3) / 1e9, "bytes_per_launch": by,
-            "kernel": "gla_chunk_bwd (layer_bf16, SIMT f32 FMA, three recurrences)"}
-
-
-def fp32_fma_peak_tflops():
-    """f32 FMA peak from unit counts and clocks: 128 FP32 lanes per SM, 2 FLOP per FMA, max SM clock."""
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    mhz = 2070.0
-    try:
-        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits",
-                              f"--id={torch.cuda.current_device()}"], capture_output=True, text=True, timeout=10)
-        mhz = float(out.stdout.strip().splitlines()[0])
-    except Exception:
-        pass
-    return sms * 128 * 2 * mhz * 1e6 / 1e12
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": by,
+                         "tensor": {"achieved_tflops": tfl, "peak_tflops": peaks["bf16_tflops"],
+                                    "frac": tfl / peaks["bf16_tflops"], "flops_per_launch": fl}},
+            "kernel": "gla_chunk_bwd (layer_bf16): two tensor-core state passes + chunk-parallel gradient kernel"}
 
 
 def run_e2e(args, P, D, w, wd, out, hT, dout, stream):

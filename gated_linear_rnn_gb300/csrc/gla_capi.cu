@@ -32,7 +32,12 @@ int simt_chunk_bwd_f32(const float *, const float *, const float *, const float 
 int simt_chunk_bwd_bf16(const void *, const void *, const void *, const void *, const float *, const float *,
                         const float *, void *, void *, void *, float *, int, int, int, int, int, int,
                         const int32_t *, cudaStream_t);
+bool tc_bwd_supported(int dk, int dv, int chunk);
+int tc_chunk_bwd_bf16(const void *, const void *, const void *, const void *, const float *, const float *,
+                      const float *, void *, void *, void *, float *, int, int, int, int, int, const int32_t *,
+                      cudaStream_t);
 int take_status_simt(cudaStream_t);
+int take_status_bwd(cudaStream_t);
 int take_status_decode(cudaStream_t);
 int take_status_tc(cudaStream_t);
 
@@ -152,6 +157,9 @@ int gla_chunk_bwd(const void *q, const void *k, const void *v, const void *dout,
                   int H, int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream) {
     int rc = check_backward(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, cu_seqlens);
     if (rc) return rc;
+    if (chunk == 128 && tc_bwd_supported(dk, dv, chunk))
+        return tc_chunk_bwd_bf16(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv,
+                                 cu_seqlens, (cudaStream_t)stream);
     return simt_chunk_bwd_bf16(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, chunk,
                                cu_seqlens, (cudaStream_t)stream);
 }
@@ -193,7 +201,7 @@ int gla_decode_step_paged(const void *q, const void *k, const void *v, const flo
 int gla_last_device_status(void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     int result = GLA_OK;
-    const int parts[3] = {take_status_simt(st), take_status_decode(st), take_status_tc(st)};
+    const int parts[4] = {take_status_simt(st), take_status_decode(st), take_status_tc(st), take_status_bwd(st)};
     for (int p : parts) {
         if (p == GLA_ERR_LAUNCH) return GLA_ERR_LAUNCH;
         if (result == GLA_OK && p != 0) result = p;

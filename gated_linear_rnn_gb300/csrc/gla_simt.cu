@@ -61,6 +61,7 @@ enum : int {
     kH0Transposed = 1,  // h0 is stored [dv][dk] per chain: S[d][c] = h0[c][d]
     kH0Undecayed = 2,   // h0 enters the first step without its decay: S_1 = h0 + k_1^T v_1
     kHTTimesDecay = 4,  // hT is written as lambda * S_T
+    kStrongOnly = 8,    // only heads with log_decay < -0.3 (the others are left untouched)
 };
 
 template <typename T, int C, bool Rev>
@@ -89,6 +90,7 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
 
     // powers of lambda: tab[n] = lambda^n, n = 0..C
     const float ld = __ldg(log_decay + h);
+    if ((state_mode & kStrongOnly) && ld >= -0.3f) return;  // served by the tensor-core backward
     for (int n = tid; n <= C; n += kThreads) tab[n] = expf((float)n * ld);
 
     // state tile: S[d][c] for c < dvt (columns beyond nc kept at zero)
@@ -300,21 +302,31 @@ int simt_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float
 template <typename T>
 int simt_bwd(const T *q, const T *k, const T *v, const T *dout, const float *ld, const float *h0, const float *dhT,
              T *dq, T *dk_, T *dv_, float *dh0, int nseq, int Tlen, int H, int dk, int dv, int chunk,
-             const int32_t *cu, cudaStream_t st) {
+             const int32_t *cu, cudaStream_t st, int extra = 0) {
     int rc = launch_simt<T, true>(k, q, dout, ld, dhT, dv_, dh0, nseq, Tlen, H, dk, dv, chunk, cu, st,
-                                  kH0Undecayed | kHTTimesDecay);
+                                  kH0Undecayed | kHTTimesDecay | extra);
     if (rc != GLA_OK) return rc;
     rc = launch_simt<T, true>(v, dout, q, ld, dhT, dk_, nullptr, nseq, Tlen, H, dv, dk, chunk, cu, st,
-                              kH0Undecayed | kH0Transposed);
+                              kH0Undecayed | kH0Transposed | extra);
     if (rc != GLA_OK) return rc;
     return launch_simt<T, false>(dout, v, k, ld, h0, dq, nullptr, nseq, Tlen, H, dv, dk, chunk, cu, st,
-                                 kH0Transposed);
+                                 kH0Transposed | extra);
 }
 
 int simt_chunk_bwd_f32(const float *q, const float *k, const float *v, const float *dout, const float *ld,
                        const float *h0, const float *dhT, float *dq, float *dk_, float *dv_, float *dh0, int nseq,
                        int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st) {
     return simt_bwd<float>(q, k, v, dout, ld, h0, dhT, dq, dk_, dv_, dh0, nseq, Tlen, H, dk, dv, chunk, cu, st);
+}
+
+// The SIMT backward for the heads with log_decay < -0.3 only (companion of the tensor-core backward).
+int simt_chunk_bwd_bf16_strong(const void *q, const void *k, const void *v, const void *dout, const float *ld,
+                               const float *h0, const float *dhT, void *dq, void *dk_, void *dv_, float *dh0,
+                               int nseq, int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu,
+                               cudaStream_t st) {
+    using B = __nv_bfloat16;
+    return simt_bwd<B>((const B *)q, (const B *)k, (const B *)v, (const B *)dout, ld, h0, dhT, (B *)dq, (B *)dk_,
+                       (B *)dv_, dh0, nseq, Tlen, H, dk, dv, chunk, cu, st, kStrongOnly);
 }
 
 int simt_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *dout, const float *ld,

@@ -75,7 +75,14 @@ constexpr uint64_t kWaitBudgetNs = 4000000000ull;  // 4 s per wait
 // segments of seg_chunks chunks: pass 1 (kStateOnly) computes every segment's end state from a zero
 // start, a small scan turns those into the segment start states, and pass 2 (kSegmented) runs the
 // full forward of every segment from its start state.
-enum Mode : int { kWhole = 0, kStateOnly = 1, kSegmented = 2 };
+//
+// kStates is the state pass of the backward: a state-only walk over whole chains, forwards or
+// backwards in time, that also writes the state in force before every chunk (the bf16 tile MMA3
+// would read, as a raw shared-memory image) to chunk_states.  Forwards it gives the S_{c-1} of the
+// chunks from h0; backwards, with the tiles of q and dout in the roles of k and v, it gives the
+// gradient states G_c = dL/dS_c from dhT:  G_{c-1} = lambda^L G_c + sum_i lambda^(i+1) q_i^T do_i,
+// and dh0 as its final state.
+enum Mode : int { kWhole = 0, kStateOnly = 1, kSegmented = 2, kStates = 3 };
 
 struct Params {
     const float *log_decay;
@@ -90,6 +97,9 @@ struct Params {
     int grid_seg;          // segments per chain in this launch (nseg - 1 for kStateOnly)
     const float *seg_h0;   // kSegmented: start states of segments 1..nseg-1, [chains, nseg-1, dk, dv]
     float *seg_end;        // kStateOnly: end states of segments 0..nseg-2 from zero, [chains, nseg-1, dk, dv]
+    int reverse;           // kStates: walk the chunks backwards in time (launches the kRev kernel)
+    __nv_bfloat16 *chunk_states;  // kStates: [slots, H, dk*dv] state images; chunk c of sequence s at
+                                  // slot start_s / 128 + s + c (start_s its first row)
 };
 
 // Shared memory plan (bytes from the 1024-aligned base).
@@ -156,6 +166,9 @@ __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, fl
     }
 }
 
+// kRev: the reversed state pass of the backward (kStates with reverse set); a separate instantiation
+// so that the forward's register allocation is untouched.
+template <bool kRev>
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -179,13 +192,15 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chain = blockIdx.x / P.grid_seg, seg = blockIdx.x % P.grid_seg;
     const int seq = chain / H, h = chain % H;
-    const bool state_only = P.mode == kStateOnly;
+    const bool state_only = P.mode == kStateOnly || P.mode == kStates;
+    constexpr bool rev = kRev;
+    const bool write_images = P.mode == kStates && P.chunk_states != nullptr;
 
     SeqRange rng;
     const bool valid = seq_range(seq, P.T, P.cu, rng);
     int64_t len = valid ? rng.len : 0;
     int64_t start = rng.start;
-    if (P.mode != kWhole) {  // one segment of a dense sequence
+    if (P.mode == kStateOnly || P.mode == kSegmented) {  // one segment of a dense sequence
         const int64_t s0 = (int64_t)seg * P.seg_chunks * kC;
         start += s0;
         len = (len - s0 < (int64_t)P.seg_chunks * kC) ? len - s0 : (int64_t)P.seg_chunks * kC;
@@ -216,6 +231,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const int64_t rem = len - (int64_t)c * kC;
         return (int)(rem < kC ? rem : kC);
     };
+    // the c-th chunk walked (backwards in time for a reversed state pass) and its length
+    auto nat = [&](int c) -> int { return rev ? nchunks - 1 - c : c; };
+    auto plen = [&](int c) -> int { return chunk_len(nat(c)); };
 
     if (threadIdx.x == 0) {
         if (!valid) record_status(GLA_ERR_DEVICE_ARG);
@@ -263,7 +281,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = c & 1;
-                const int y = row0 + c * kC;
+                const int y = row0 + nat(c) * kC;
                 if (c >= 2) ok = mbar_wait(BAR(B_KVEMPTY0 + s), ((c >> 1) - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 mbar_expect_tx(BAR(B_KVFULL0 + s), kvbytes);
@@ -292,6 +310,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint32_t id_kv = idesc_bf16(kC, dv, 1, 1);
             const int ksteps_dk = dk / 16;
             const uint32_t qbuf = sbase + o_q, sbuf = sbase + o_s;
+            // image of the state before chunk 0 of this chain (slot start / 128 + seq; chunk c adds c slots)
+            __nv_bfloat16 *const img0 =
+                write_images ? P.chunk_states + ((rng.start / kC + seq) * H + h) * sz_state : nullptr;
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = c & 1;
@@ -303,6 +324,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                          mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);
                     if (!ok) break;
                     tc_fence_after();
+                    if (write_images) {
+                        // the state in force before chunk nat(c), as the bf16 tile the state pass just
+                        // wrote: copy it out, and let it be read before MMA4 (and so before the next state
+                        // pass may refill it)
+                        bulk_store_s2g(img0 + (int64_t)nat(c) * H * sz_state, sbase + o_s, (uint32_t)(sz_state * 2));
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
                     for (int kk = 0; kk < kC / 16; ++kk) {
                         mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
                                smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
@@ -375,8 +404,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const bool early_k = fact || state_only;
         auto prep_k_early = [&](int c) -> bool {
             if (!mbar_wait(BAR(B_KVFULL0 + (c & 1)), (c >> 1) & 1, abort_flag, kWaitBudgetNs)) return false;
-            const int Lk = chunk_len(c);
-            const float f = (r < Lk) ? (fact ? utab[r] : tab[Lk - 1 - r]) : 0.f;
+            const int Lk = plen(c);
+            // forwards: lambda^-(j+1) (factored) or lambda^(L-1-j); backwards in time the weight of row i
+            // is lambda^(i+1): lambda^(i+1-L) in the factored form (the state is scaled by lambda^L after)
+            const float fw = fact ? utab[r] : tab[Lk - 1 - r];
+            const float bw = fact ? tab[min(r + 1, kC)] * utab[Lk - 1] : tab[min(r + 1, kC)];
+            const float f = (r < Lk) ? (rev ? bw : fw) : 0.f;
             scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, f);
             fence_async_shared();
             __syncwarp();
@@ -393,9 +426,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const bool last = (c == nchunks);
             // factored: TMEM holds S_{c-2} + K''^T V, S_{c-1} = lambda^L(c-1) * that; copy and TMEM both get it.
             // direct:   TMEM holds S_{c-1}; the copy is S_{c-1}, TMEM gets lambda^L(c) S_{c-1} for MMA4.
-            const float g_prev = (fact && c >= 1) ? tab[chunk_len(c - 1)] : 1.f;
+            const float g_prev = (fact && c >= 1) ? tab[plen(c - 1)] : 1.f;
             const float g_copy = g_prev;
-            const float g_tmem = fact ? g_prev : (last ? 1.f : tab[chunk_len(c)]);
+            const float g_tmem = fact ? g_prev : (last ? 1.f : tab[plen(c)]);
             if (r < dk) {
                 // two 32-column groups per step: both TMEM loads in flight before the first use
                 for (int j0 = 0; j0 < dv; j0 += 64) {
@@ -435,7 +468,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     // bf16 copy into the MN-major, 128B-swizzled S tile: one 64-column atom
                     uint8_t *atom_row = smem + o_s + (uint32_t)(j0 >> 6) * (uint32_t)dk * 128u + (uint32_t)r * 128u;
 #pragma unroll
-                    for (int q8 = 0; q8 < 8 && !state_only; ++q8) {
+                    for (int q8 = 0; q8 < 8 && (!state_only || write_images); ++q8) {
                         const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
                         *reinterpret_cast<uint4 *>(atom_row + (((uint32_t)q8 ^ (uint32_t)(r & 7)) << 4)) =
                             make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
@@ -679,8 +712,11 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
+// 2-D bf16 tensor map over [rows, cols] (row stride cols * 2 bytes) with a box of box_rows x box_cols.
 bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              CUtensorMapSwizzle sw, uint32_t box_rows = kC) {
+              CUtensorMapSwizzle sw, uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -692,6 +728,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              CUtensorMapSwizzle sw) {
+    return gla::make_map(m, base, cols, rows, box_cols, sw, kC);
+}
 }  // namespace
 
 bool tc_chunk_supported(int dk, int dv, int chunk) {
@@ -724,7 +765,14 @@ int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &m
               const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    gla_tc_chunk_kernel<<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    if (p.reverse) {
+        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes) != cudaSuccess)
+            return GLA_ERR_LAUNCH;
+        gla_tc_chunk_kernel<true><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    } else {
+        gla_tc_chunk_kernel<false><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    }
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -744,10 +792,10 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
         return GLA_ERR_LAUNCH;
     const Smem sp = smem_plan(dk, dv);
     const size_t bytes = sp.total + 1024;  // + alignment slack
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
         return GLA_ERR_LAUNCH;
-    Params p;
+    Params p{};
     p.log_decay = ld;
     p.h0 = h0;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
@@ -796,6 +844,45 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     }
     cudaFreeAsync(scratch, st);
     return rc;
+}
+
+// ---- state passes of the backward ------------------------------------------------------
+// One state-only walk over every (sequence, head) chain with the tiles of `ka` ([rows, H, dk], in the
+// role of k) and `va` ([rows, H, dv], in the role of v): forwards from `init` (or zeros), or backwards
+// in time (reverse != 0).  The bf16 state in force before every chunk goes to `images`
+// ([slots, H, dk, dv], chunk c of sequence s at slot start_s / 128 + s + c); the final state to
+// `final_` if given.  Forwards with (k, v) this yields the S_{c-1}; backwards with (q, dout) from dhT
+// the gradient states G_c and dh0.
+int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const float *init, float *final_,
+                       void *images, int reverse, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu,
+                       cudaStream_t st) {
+    if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
+    const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
+    if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, ka, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&mv, va, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return GLA_ERR_LAUNCH;
+    const size_t bytes = smem_plan(dk, dv).total + 1024;
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return GLA_ERR_LAUNCH;
+    Params p{};
+    p.log_decay = ld;
+    p.h0 = init;
+    p.hT = final_;
+    p.cu = cu;
+    p.T = Tlen;
+    p.H = H;
+    p.dk = dk;
+    p.dv = dv;
+    p.mode = kStates;
+    p.nseg = 1;
+    p.grid_seg = 1;
+    p.reverse = reverse ? 1 : 0;
+    p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
+    // the q and out maps are not read in a state-only pass
+    return launch_tc(mk, mk, mv, mv, p, (long long)nseq * H, bytes, st);
 }
 
 // ---- no-alloc variant ------------------------------------------------------------
@@ -856,10 +943,10 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
         !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
         return GLA_ERR_LAUNCH;
     const size_t bytes = smem_plan(dk, dv).total + 1024;
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
         return GLA_ERR_LAUNCH;
-    Params p;
+    Params p{};
     p.log_decay = ld;
     p.h0 = h0;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);

@@ -82,6 +82,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, int32_t x, in
                  ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
+// Bulk copy shared -> global (no tensor map): 16-byte aligned addresses, size a multiple of 16.
+__device__ __forceinline__ void bulk_store_s2g(void *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(gdst)), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+// Bulk copy global -> shared (no tensor map), completing on an mbarrier with its byte count.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void *gsrc, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(sdst), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until the shared-memory sources of all committed bulk stores have been read
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

@@ -167,9 +167,15 @@ GLA_API int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, co
  *   dv           [B, T, H, dv] bf16, written
  *   dh0          [B|N, H, dk, dv] f32, written; NULL to skip
  *   B, T, H, dk, dv, chunk, cu_seqlens, stream: as gla_chunk_fwd
- * Runs on the SIMT kernel (f32 accumulation): chunk in {16, 32, 64, 128};
- * chunks whose tiles do not fit in shared memory run as shorter sub-chunks.
- * No pointer may alias another.  Returns a gla_status; no scratch is taken.
+ * With chunk == 128, 32 | dk <= 128, 64 | dv <= 192 and dv + 2 dk <= 384 it
+ * runs on the tensor cores: two state passes (S before every chunk from h0,
+ * forwards; the gradient state G at every chunk's end from dhT, backwards;
+ * both kept as bf16 tiles in stream-ordered scratch of 2 x 2 dk dv bytes per
+ * chunk, GLA_ERR_NOMEM if it cannot be had) and one kernel over all (chunk,
+ * head) pairs at once.  Heads with log_decay < -0.3, and every other shape or
+ * chunk in {16, 32, 64}, run three chunked recurrences on the SIMT kernel
+ * (f32 accumulation; dv and dk backwards in time from dhT, dq forwards from
+ * h0).  No pointer may alias another.  Returns a gla_status.
  */
 GLA_API int gla_chunk_bwd(const void *q, const void *k, const void *v, const void *dout, const float *log_decay,
                           const float *h0, const float *dhT, void *dq, void *dk_out, void *dv_out, float *dh0,

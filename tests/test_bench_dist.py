@@ -65,7 +65,7 @@ def test_algorithmic_counts():
 
 def test_backward_counts():
     import bench
-    # three passes, each three token tensors read and one written: 3 x 1,152 B per token-head (bf16)
-    assert bench.backward_bytes(1, 1, 1, 96, 192) == 3 * 1152
-    # dv pass at C = 128 (dk x dv state), dk and dq passes as 64-token sub-chunks (dv x dk state)
-    assert bench.backward_flops(1, 1, 1, 96, 192, 128) == (128 * 288 + 4 * 96 * 192) + 2 * (64 * 288 + 4 * 96 * 192)
+    # state passes read k, v and q, dout; the gradient kernel reads q, k, v, dout and writes dq, dk, dv;
+    # two bf16 96 x 192 state tiles per 128-token chunk, written and read once: 4,224 B per token-head
+    assert bench.backward_bytes(1, 1, 1, 96, 192) == 4 * 288 + 4 * 288 + 2 * 384 + 8 * 96 * 192 // 128 == 4224
+    assert bench.backward_flops(1, 1, 1, 96, 192, 128) == 4 * 128 * 192 + 6 * 128 * 288 + 6 * 96 * 192

@@ -93,7 +93,8 @@ __host__ __device__ inline BwdSmem bwd_plan(int dk, int dv) {
     return p;
 }
 
-enum { B_LOAD = 0, B_MMA, B_MASK, B_FINAL };
+// loads land in three groups so that MMA1 can start on Q, K alone
+enum { B_LOAD = 0, B_LOAD2, B_LOAD3, B_MMA, B_MASK, B_FINAL };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -132,6 +133,33 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
     tmem_wait_st();
 }
 
+// Row r of an accumulator of `ncols` columns at tcol, times f, as bf16 into a staging tile laid out as
+// the TMA box of the output: 64-column atoms of 128-byte rows with the 128B swizzle (atom_cols 64), or
+// 32-column atoms of 64-byte rows with the 64B swizzle (atom_cols 32).
+__device__ __forceinline__ void stage_row(uint32_t tcol, int ncols, float f, int r, uint8_t *tile, int atom_cols) {
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(tcol + (uint32_t)c0, a);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint8_t *dst;
+            if (atom_cols == 64) {
+                const uint32_t phys = ((uint32_t)(((c0 & 63) >> 3) + q)) ^ ((uint32_t)r & 7u);
+                dst = tile + (uint32_t)(c0 >> 6) * 16384u + (uint32_t)r * 128u + (phys << 4);
+            } else {
+                const uint32_t phys = (uint32_t)q ^ (((uint32_t)r >> 1) & 3u);
+                dst = tile + (uint32_t)(c0 >> 5) * 8192u + (uint32_t)r * 64u + (phys << 4);
+            }
+            *reinterpret_cast<uint4 *>(dst) =
+                make_uint4(pack_bf16x2(__uint_as_float(a[8 * q]) * f, __uint_as_float(a[8 * q + 1]) * f),
+                           pack_bf16x2(__uint_as_float(a[8 * q + 2]) * f, __uint_as_float(a[8 * q + 3]) * f),
+                           pack_bf16x2(__uint_as_float(a[8 * q + 4]) * f, __uint_as_float(a[8 * q + 5]) * f),
+                           pack_bf16x2(__uint_as_float(a[8 * q + 6]) * f, __uint_as_float(a[8 * q + 7]) * f));
+        }
+    }
+}
+
 // Row r of an accumulator of `ncols` columns at tcol, times f, as bf16 into dst (global), if r < L.
 __device__ __forceinline__ void store_row(uint32_t tcol, int ncols, float f, bool live, __nv_bfloat16 *dst) {
     for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -153,7 +181,8 @@ __device__ __forceinline__ void store_row(uint32_t tcol, int ncols, float f, boo
 __global__ void __launch_bounds__(kThreads, 1)
 gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                  const BwdParams P) {
+                  const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                  const __grid_constant__ CUtensorMap tmDV, const BwdParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int dk = P.dkk, dv = P.dvv, H = P.H;
@@ -201,6 +230,8 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(BAR(B_LOAD), 1);
+        mbar_init(BAR(B_LOAD2), 1);
+        mbar_init(BAR(B_LOAD3), 1);
         mbar_init(BAR(B_MMA), 1);
         mbar_init(BAR(B_MASK), 4);
         mbar_init(BAR(B_FINAL), 1);
@@ -227,19 +258,24 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmDQ);
+        tma_prefetch_desc(&tmDK);
+        tma_prefetch_desc(&tmDV);
         const uint32_t st_bytes = (uint32_t)dk * dv * 2u;
-        mbar_expect_tx(BAR(B_LOAD), 2u * nka * 8192u + 2u * nva * 16384u + 2u * st_bytes);
         const int y = (int)row0;
+        mbar_expect_tx(BAR(B_LOAD), 2u * nka * 8192u);
         for (int a = 0; a < nka; ++a) {
             tma_load_2d(sb + plan.q + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(B_LOAD));
             tma_load_2d(sb + plan.k + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(B_LOAD));
         }
+        mbar_expect_tx(BAR(B_LOAD2), 2u * nva * 16384u + st_bytes);
         for (int a = 0; a < nva; ++a) {
-            tma_load_2d(sb + plan.v + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(B_LOAD));
-            tma_load_2d(sb + plan.dout + a * 16384u, &tmDO, h * dv + 64 * a, y, BAR(B_LOAD));
+            tma_load_2d(sb + plan.v + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(B_LOAD2));
+            tma_load_2d(sb + plan.dout + a * 16384u, &tmDO, h * dv + 64 * a, y, BAR(B_LOAD2));
         }
-        bulk_load_g2s(sb + plan.s, P.s_img + img, st_bytes, BAR(B_LOAD));
-        bulk_load_g2s(sb + plan.g, P.g_img + img, st_bytes, BAR(B_LOAD));
+        bulk_load_g2s(sb + plan.g, P.g_img + img, st_bytes, BAR(B_LOAD2));
+        mbar_expect_tx(BAR(B_LOAD3), st_bytes);
+        bulk_load_g2s(sb + plan.s, P.s_img + img, st_bytes, BAR(B_LOAD3));
     }
 
     // descriptors
@@ -264,9 +300,14 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const uint32_t id_vg = idesc_bf16(kC, dk, 0, 0);    // [tokens x dv] (K-major) x image^T (K-major, N = dk)
     const uint32_t vatom = 16384u, iatom = (uint32_t)dk * 128u;
 
-    bool ok = mbar_wait(BAR(B_LOAD), 0, abort_flag, kWaitBudgetNs);
-    if (!ok) *abort_flag = 1;  // every other wait of this CTA then gives up at once
-    tc_fence_after();
+    bool ok = true;
+    // only the MMA issuer waits for loads; a failed wait sets the abort flag, which ends every other
+    // wait of this CTA at once
+    auto wait_load = [&](int b) {
+        ok = ok && mbar_wait(BAR(b), 0, abort_flag, kWaitBudgetNs);
+        if (!ok) *abort_flag = 1;
+    };
+    if (tid == 0) wait_load(B_LOAD);
     // ---- MMA1: A^T = K Q^T ----
     if (ok && tid == 0) {
         for (int kk = 0; kk < dk / 16; ++kk) mma_ss(tmem + kColScratch, kmaj64(kb, kk), kmaj64(qb, kk), id_tt, kk > 0);
@@ -301,6 +342,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     masked(false, wcol);
     if (tid == 0) {
         wait_mask();
+        wait_load(B_LOAD2);
         if (ok) {
             // MMA2: dV = P1 dO + K G_c
             for (int kk = 0; kk < kC / 16; ++kk)
@@ -333,6 +375,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     masked(true, utab);
     if (tid == 0) {
         wait_mask();
+        wait_load(B_LOAD3);
         if (ok) {
             // MMA6: dQ = P3 K + dO S_{c-1}^T
             for (int kk = 0; kk < kC / 16; ++kk)
@@ -344,15 +387,37 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     wait_mma();
 
     // ---- epilogue: row factors, bf16, rows below L ----
+    ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA: the epilogue has a barrier
     if (ok) {
         const int r = tid;
-        const bool live = r < L;
-        const int64_t row = row0 + (r < L ? r : 0);
         const float rf = tab[max(L - 1 - r, 0)];  // lambda^(L-1-j) for dV and dK
         const float qf = tab[min(r + 1, kC)];     // lambda^(i+1) for dQ
-        store_row(tmem + lane_base + colDV, dv, rf, live, P.dv + (row * H + h) * dv);
-        store_row(tmem + lane_base + colDK, dk, rf, live, P.dk + (row * H + h) * dk);
-        store_row(tmem + lane_base + colDQ, dk, qf, live, P.dq + (row * H + h) * dk);
+        if (L == kC) {
+            // a full chunk: every tile is free now; stage the rows as TMA boxes (dV over V, dK over K,
+            // dQ over Q) and write them with one store per atom
+            stage_row(tmem + lane_base + colDV, dv, rf, r, smem + plan.v, 64);
+            stage_row(tmem + lane_base + colDK, dk, rf, r, smem + plan.k, 32);
+            stage_row(tmem + lane_base + colDQ, dk, qf, r, smem + plan.q, 32);
+            fence_async_shared();
+            __syncthreads();
+            if (tid == 0) {
+                const int y = (int)row0;
+                for (int a = 0; a < nva; ++a) tma_store_2d(&tmDV, h * dv + 64 * a, y, vb + a * 16384u);
+                for (int a = 0; a < nka; ++a) {
+                    tma_store_2d(&tmDK, h * dk + 32 * a, y, kb + a * 8192u);
+                    tma_store_2d(&tmDQ, h * dk + 32 * a, y, qb + a * 8192u);
+                }
+                bulk_commit();
+                bulk_wait_read0();  // the stores must have read shared memory before the CTA exits
+            }
+        } else {
+            // the last chunk of a sequence: rows from L on belong to the next one; plain stores
+            const bool live = r < L;
+            const int64_t row = row0 + (r < L ? r : 0);
+            store_row(tmem + lane_base + colDV, dv, rf, live, P.dv + (row * H + h) * dv);
+            store_row(tmem + lane_base + colDK, dk, rf, live, P.dk + (row * H + h) * dk);
+            store_row(tmem + lane_base + colDQ, dk, qf, live, P.dq + (row * H + h) * dk);
+        }
     } else if (tid == 0) {
         record_status(GLA_ERR_TIMEOUT);
     }
@@ -392,11 +457,14 @@ int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *d
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
     const long long slots = (long long)(rows / kC) + nseq + 1;
     if (slots * H > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo, mdq, mdk, mdv;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B, kC) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B, kC) ||
         !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC) ||
-        !make_map(&mo, dout, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC))
+        !make_map(&mo, dout, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC) ||
+        !make_map(&mdq, dq, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B, kC) ||
+        !make_map(&mdk, dk_, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B, kC) ||
+        !make_map(&mdv, dv_, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC))
         return GLA_ERR_LAUNCH;
     const size_t per = (size_t)slots * H * dk * dv;  // bf16 elements per image array
     __nv_bfloat16 *img = nullptr;
@@ -426,7 +494,7 @@ int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *d
             p.dkk = dk;
             p.dvv = dv;
             p.slots = (int)slots;
-            gla_bwd_tc_kernel<<<(unsigned)(slots * H), kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+            gla_bwd_tc_kernel<<<(unsigned)(slots * H), kThreads, bytes, st>>>(mq, mk, mv, mo, mdq, mdk, mdv, p);
             count_launches(1);
             rc = cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
         }

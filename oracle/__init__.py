@@ -63,6 +63,8 @@ def _load():
             lib.gla_oracle_decode_step.restype = I
             lib.gla_oracle_backward.argtypes = [P] * 13 + [I, I, I, I, P, I, I]
             lib.gla_oracle_backward.restype = I
+            lib.gla_oracle_conv1d_silu.argtypes = [P] * 8 + [I, I]
+            lib.gla_oracle_conv1d_silu.restype = I
             _lib = lib
     return _lib
 
@@ -185,6 +187,41 @@ def backward(q, k, v, dout, log_decay, h0=None, dhT=None, cu_seqlens=None, units
     if rc != 0:
         raise ValueError("oracle backward rejected its arguments")
     return dq, dkk, dvv, dh0
+
+
+def conv1d_silu(x, weight, bias=None, state=None, cu_seqlens=None):
+    """Causal depthwise Conv1d (width 4) + SiLU per channel ([L3B] "i14 与 Laplace 3B 架构").
+
+    x: [B, T, D] (or packed [1, T, D] with ``cu_seqlens``); weight [D, 4] (weight[:, 3] meets the
+    current token); bias [D] or None; state [nseq, D, 3] (the three inputs before each sequence,
+    oldest first) or None.  Returns (y [B, T, D] float64, state_out [nseq, D, 3] float64)."""
+    x = _f32(x)
+    if x.ndim != 3:
+        raise ValueError("x must be [B, T, D]")
+    B, T, D = x.shape
+    w = _f64(weight)
+    if w.shape != (D, 4):
+        raise ValueError("weight must be [D, 4]")
+    b = None if bias is None else _f64(bias).reshape(D)
+    if cu_seqlens is None:
+        starts = np.arange(B, dtype=np.int64) * T
+        lens = np.full(B, T, dtype=np.int64)
+    else:
+        if B != 1:
+            raise ValueError("a packed batch has leading dimension 1")
+        cu = np.asarray(cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64)
+        starts, lens = cu[:-1].copy(), np.diff(cu)
+    nseq = starts.shape[0]
+    st = None if state is None else _f64(state)
+    if st is not None and st.shape != (nseq, D, 3):
+        raise ValueError(f"state must be {(nseq, D, 3)}")
+    y = np.zeros((B, T, D), dtype=np.float64)
+    so = np.zeros((nseq, D, 3), dtype=np.float64)
+    rc = _load().gla_oracle_conv1d_silu(_ptr(x), _ptr(w), _ptr(b), _ptr(st), _ptr(so), _ptr(y), _ptr(starts),
+                                        _ptr(lens), nseq, D)
+    if rc != 0:
+        raise ValueError("oracle conv1d rejected its arguments")
+    return y, so
 
 
 def decode_step(q, k, v, log_decay, state, nthreads=None):

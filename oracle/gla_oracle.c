@@ -457,3 +457,45 @@ int gla_oracle_backward(const float *q, const float *k, const float *v, const fl
     for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
     return J.error ? -1 : 0;
 }
+
+/*
+ * Causal depthwise Conv1d of width 4 followed by SiLU, per channel
+ * ([L3B] §"i14 与 Laplace 3B 架构", "归一化与卷积": every position of the
+ * normalised residual stream gets a 4-token summary from a per-channel causal
+ * convolution of width k = 4 with SiLU, before the QKVG projection).  The page
+ * prints no formula; the reading taken here, for channel c at token t:
+ *   z = b[c] + sum_{k=0..3} w[c][k] * x_{t-3+k}[c]       (w[c][3] meets x_t)
+ *   y_t[c] = z / (1 + exp(-z))                           (SiLU)
+ * where x before a sequence's first token comes from its conv state
+ * (state[s][c][m] = x_{m-3}[c], m = 0..2, oldest first; NULL = zeros).  The
+ * state after the sequence holds its last three inputs (earlier ones from the
+ * incoming state when the sequence is shorter than three).
+ *   x, y  : [rows, D] float32 in, float64 out;  w : [D, 4];  b : [D] or NULL
+ *   state_in / state_out : [nseq, D, 3] float64 or NULL
+ */
+int gla_oracle_conv1d_silu(const float *x, const double *w, const double *b, const double *state_in,
+                           double *state_out, double *y, const int64_t *seq_start, const int64_t *seq_len,
+                           int nseq, int D) {
+    if (!x || !w || !y || !seq_start || !seq_len || nseq < 0 || D <= 0) return -1;
+    for (int s = 0; s < nseq; ++s) {
+        if (seq_len[s] < 0 || seq_start[s] < 0) return -1;
+        const int64_t r0 = seq_start[s], T = seq_len[s];
+        for (int c = 0; c < D; ++c) {
+            double hist[3];  /* x_{t-3}, x_{t-2}, x_{t-1} */
+            for (int m = 0; m < 3; ++m) hist[m] = state_in ? state_in[((size_t)s * D + c) * 3 + m] : 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                const double xt = (double)x[(size_t)(r0 + t) * D + c];
+                double z = b ? b[c] : 0.0;
+                for (int k = 0; k < 3; ++k) z += w[(size_t)c * 4 + k] * hist[k];
+                z += w[(size_t)c * 4 + 3] * xt;
+                y[(size_t)(r0 + t) * D + c] = z / (1.0 + exp(-z));
+                hist[0] = hist[1];
+                hist[1] = hist[2];
+                hist[2] = xt;
+            }
+            if (state_out)
+                for (int m = 0; m < 3; ++m) state_out[((size_t)s * D + c) * 3 + m] = hist[m];
+        }
+    }
+    return 0;
+}

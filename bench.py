@@ -348,6 +348,9 @@ def run_ours(args, world, rank, local):
     # ---- paged decode: the same step through a slot table (a permutation of the state pages) ----
     paged = run_paged_decode(args, D, wd, dout, stream, peaks)
 
+    # ---- causal conv1d + SiLU over the layer's residual stream, and its per-token step ----
+    conv = run_conv(args, w, wd, stream, peaks, dev)
+
     # ---- backward of the layer prefill (training path), timed on its own after the step ----
     bwd = run_backward(args, P, w, stream, peaks, peak_src) if args.bwd_steps > 0 else None
 
@@ -373,6 +376,7 @@ def run_ours(args, world, rank, local):
                    "tokens_per_s": wd.B * world / dec_avg_s},
         "e2e": e2e,
         "decode_paged": paged,
+        "conv1d_silu": conv,
         "backward": bwd,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -416,6 +420,47 @@ def run_paged_decode(args, D, wd, dout, stream, peaks):
     return {"us_per_step": us, "unit": "state GB/s", "value": sbytes / (us / 1e6) / 1e9,
             "frac_of_hbm_peak": (sbytes + iobytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"], "steps": n,
             "rows": wd.B, "pool_pages": wd.B}
+
+
+def run_conv(args, w, wd, stream, peaks, dev, D=3072):
+    """gla_conv1d_silu over [B, T, D] bf16 (the layer's residual stream, D = 3072) and
+    gla_conv1d_silu_step over [N, D] with the decode workload's N; CUDA events, median."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    g = torch.Generator(device=dev).manual_seed(11)
+    x = torch.randn(w.B, w.T, D, generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    wt = torch.randn(D, 4, generator=g, device=dev) * 0.5
+    bias = torch.randn(D, generator=g, device=dev) * 0.1
+    so = torch.empty(w.B, D, 3, device=dev)
+    xs = torch.randn(wd.B, D, generator=g, device=dev).to(torch.bfloat16)
+    ys = torch.empty_like(xs)
+    st = torch.zeros(wd.B, D, 3, device=dev)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for e in ev:
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+
+    n = max(3, min(args.steps, 50))
+    ms = timed(lambda: gla.gla_conv1d_silu(x, wt, bias, None, so, y, None, stream), n)
+    ms_step = timed(lambda: gla.gla_conv1d_silu_step(xs, wt, bias, st, ys, stream), n)
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the conv: {st_code} ({gla.gla_status_str(st_code)})")
+    by = w.B * w.T * D * 2 * 2 + D * 4 * 4 + D * 4 + w.B * D * 3 * 4
+    by_step = wd.B * D * 2 * 2 + wd.B * D * 3 * 4 * 2
+    return {"value": w.B * w.T / (ms / 1e3), "unit": "tokens/s", "us": ms * 1e3, "shape": [w.B, w.T, D],
+            "roofline": {"bound": "hbm", "achieved": by / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": by},
+            "step": {"us": ms_step * 1e3, "rows": wd.B, "gbs": by_step / (ms_step / 1e3) / 1e9,
+                     "frac_of_hbm_peak": by_step / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"]}}
 
 
 def run_backward(args, P, w, stream, peaks, peak_src):

@@ -36,6 +36,12 @@ bool tc_bwd_supported(int dk, int dv, int chunk);
 int tc_chunk_bwd_bf16(const void *, const void *, const void *, const void *, const float *, const float *,
                       const float *, void *, void *, void *, float *, int, int, int, int, int, const int32_t *,
                       cudaStream_t);
+int conv1d_silu_bf16(const void *, const float *, const float *, const float *, float *, void *, int, int, int,
+                     const int32_t *, cudaStream_t);
+int conv1d_silu_f32(const float *, const float *, const float *, const float *, float *, float *, int, int, int,
+                    const int32_t *, cudaStream_t);
+int conv1d_silu_step_bf16(const void *, const float *, const float *, float *, void *, int, int, cudaStream_t);
+int take_status_conv(cudaStream_t);
 int take_status_simt(cudaStream_t);
 int take_status_bwd(cudaStream_t);
 int take_status_decode(cudaStream_t);
@@ -97,6 +103,17 @@ int check_backward(const void *q, const void *k, const void *v, const void *dout
     if (rc) return rc;
     if (!aligned16(dhT) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dh0))
         return GLA_ERR_ALIGN;
+    return GLA_OK;
+}
+
+int check_conv(const void *x, const float *w, const float *b, const float *s_in, const float *s_out, const void *y,
+               int B, int T, int D) {
+    if (!x || !w || !y) return GLA_ERR_ARG;
+    if (B <= 0 || T <= 0 || D <= 0) return GLA_ERR_ARG;
+    if (D % 8) return GLA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(s_in) || !aligned16(s_out) || !aligned16(y))
+        return GLA_ERR_ALIGN;
+    if (!device_info().ok) return GLA_ERR_UNSUPPORTED;
     return GLA_OK;
 }
 
@@ -198,10 +215,35 @@ int gla_decode_step_paged(const void *q, const void *k, const void *v, const flo
                                   (cudaStream_t)stream);
 }
 
+int gla_conv1d_silu(const void *x, const float *weight, const float *bias, const float *state_in, float *state_out,
+                    void *y, int B, int T, int D, const int32_t *cu_seqlens, void *stream) {
+    int rc = check_conv(x, weight, bias, state_in, state_out, y, B, T, D);
+    if (rc) return rc;
+    if (!aligned16(cu_seqlens)) return GLA_ERR_ALIGN;
+    return conv1d_silu_bf16(x, weight, bias, state_in, state_out, y, B, T, D, cu_seqlens, (cudaStream_t)stream);
+}
+
+int gla_conv1d_silu_f32(const float *x, const float *weight, const float *bias, const float *state_in,
+                        float *state_out, float *y, int B, int T, int D, const int32_t *cu_seqlens, void *stream) {
+    int rc = check_conv(x, weight, bias, state_in, state_out, y, B, T, D);
+    if (rc) return rc;
+    if (!aligned16(cu_seqlens)) return GLA_ERR_ALIGN;
+    return conv1d_silu_f32(x, weight, bias, state_in, state_out, y, B, T, D, cu_seqlens, (cudaStream_t)stream);
+}
+
+int gla_conv1d_silu_step(const void *x, const float *weight, const float *bias, float *state_inout, void *y, int N,
+                         int D, void *stream) {
+    if (!state_inout) return GLA_ERR_ARG;
+    int rc = check_conv(x, weight, bias, state_inout, state_inout, y, N, 1, D);
+    if (rc) return rc;
+    return conv1d_silu_step_bf16(x, weight, bias, state_inout, y, N, D, (cudaStream_t)stream);
+}
+
 int gla_last_device_status(void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     int result = GLA_OK;
-    const int parts[4] = {take_status_simt(st), take_status_decode(st), take_status_tc(st), take_status_bwd(st)};
+    const int parts[5] = {take_status_simt(st), take_status_decode(st), take_status_tc(st), take_status_bwd(st),
+                          take_status_conv(st)};
     for (int p : parts) {
         if (p == GLA_ERR_LAUNCH) return GLA_ERR_LAUNCH;
         if (result == GLA_OK && p != 0) result = p;

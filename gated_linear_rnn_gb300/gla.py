@@ -34,6 +34,9 @@ SIGNATURES = {
     "gla_decode_step": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_paged": ([_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
+    "gla_conv1d_silu": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "gla_conv1d_silu_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P], _I),
+    "gla_conv1d_silu_step": ([_P, _P, _P, _P, _P, _I, _I, _P], _I),
     "gla_last_device_status": ([_P], _I),
     "gla_status_str": ([_I], ctypes.c_char_p),
     "gla_kernel_launches": ([], ctypes.c_uint64),
@@ -231,6 +234,55 @@ def gla_decode_step_paged(q, k, v, log_decay, state_pool, slots, out, stream=Non
     rc = load().gla_decode_step_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(state_pool), _ptr(slots),
                                       int(state_pool.shape[0]), _ptr(out), N, H, dk, dv, _stream(stream))
     _raise(rc, "gla_decode_step_paged")
+
+
+def _conv_args(x, weight, bias, state_in, state_out, y, cu_seqlens, dtype):
+    if x.dim() != 3:
+        raise ValueError("x must be [B, T, D] (packed: [1, T, D])")
+    B, T, D = x.shape
+    _check(x, "x", dtype)
+    _check(y, "y", dtype, (B, T, D))
+    _check(weight, "weight", torch.float32, (D, 4))
+    _check(bias, "bias", torch.float32, (D,), allow_none=True)
+    nseq = B
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("a packed batch has leading dimension 1")
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+        nseq = cu_seqlens.numel() - 1
+    _check(state_in, "state_in", torch.float32, (nseq, D, 3), allow_none=True)
+    _check(state_out, "state_out", torch.float32, (nseq, D, 3), allow_none=True)
+    return nseq, T, D  # the C ABI takes the number of sequences (N for a packed batch)
+
+
+def gla_conv1d_silu(x, weight, bias, state_in, state_out, y, cu_seqlens=None, stream=None) -> None:
+    """bf16 causal depthwise Conv1d (width 4) + SiLU; see include/gla.h."""
+    nseq, T, D = _conv_args(x, weight, bias, state_in, state_out, y, cu_seqlens, torch.bfloat16)
+    rc = load().gla_conv1d_silu(_ptr(x), _ptr(weight), _ptr(bias), _ptr(state_in), _ptr(state_out), _ptr(y),
+                                nseq, T, D, _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_conv1d_silu")
+
+
+def gla_conv1d_silu_f32(x, weight, bias, state_in, state_out, y, cu_seqlens=None, stream=None) -> None:
+    nseq, T, D = _conv_args(x, weight, bias, state_in, state_out, y, cu_seqlens, torch.float32)
+    rc = load().gla_conv1d_silu_f32(_ptr(x), _ptr(weight), _ptr(bias), _ptr(state_in), _ptr(state_out), _ptr(y),
+                                    nseq, T, D, _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_conv1d_silu_f32")
+
+
+def gla_conv1d_silu_step(x, weight, bias, state_inout, y, stream=None) -> None:
+    """bf16 conv step for one token of N sequences, in place on state_inout [N, D, 3]."""
+    if x.dim() != 2:
+        raise ValueError("x must be [N, D]")
+    N, D = x.shape
+    _check(x, "x", torch.bfloat16)
+    _check(y, "y", torch.bfloat16, (N, D))
+    _check(weight, "weight", torch.float32, (D, 4))
+    _check(bias, "bias", torch.float32, (D,), allow_none=True)
+    _check(state_inout, "state_inout", torch.float32, (N, D, 3))
+    rc = load().gla_conv1d_silu_step(_ptr(x), _ptr(weight), _ptr(bias), _ptr(state_inout), _ptr(y), N, D,
+                                     _stream(stream))
+    _raise(rc, "gla_conv1d_silu_step")
 
 
 def gla_last_device_status(stream=None) -> int:

@@ -238,6 +238,44 @@ GLA_API int gla_decode_step_paged(const void *q, const void *k, const void *v, c
                                   int dk, int dv, void *stream);
 
 /*
+ * gla_conv1d_silu — causal depthwise Conv1d of width 4 followed by SiLU, per
+ * channel (page "线性注意力模型如何实现固定推理状态", section "i14 与 Laplace 3B
+ * 架构", "归一化与卷积": a 4-token per-channel summary of the normalised
+ * residual stream ahead of the QKVG projection; the page prints no formula,
+ * this is the plain reading).  For channel c at token t of a sequence:
+ *     z = bias[c] + sum_{k=0..3} weight[c][k] x_{t-3+k}[c]   (weight[c][3] meets x_t)
+ *     y_t[c] = z * sigmoid(z)
+ * The three inputs before a sequence's first token come from state_in (oldest
+ * first), or are zero; state_out receives each sequence's last three inputs
+ * (for a sequence shorter than three, the newest of state_in fill the front).
+ *
+ *   x, y         [B, T, D] bf16 (packed [1, T, D] with cu_seqlens, and then B
+ *                is the number of sequences N; rows past cu_seqlens[N] are
+ *                neither read nor written)
+ *   weight       [D, 4] f32;  bias [D] f32 or NULL
+ *   state_in     [B|N, D, 3] f32 or NULL (zeros);  state_out [B|N, D, 3] f32 or NULL
+ *   D % 8 == 0; every pointer 16-byte aligned.  Memory-bound: x is read and y
+ *   written once.  Returns a gla_status.
+ */
+GLA_API int gla_conv1d_silu(const void *x, const float *weight, const float *bias, const float *state_in,
+                            float *state_out, void *y, int B, int T, int D, const int32_t *cu_seqlens,
+                            void *stream);
+
+/* gla_conv1d_silu_f32 — as gla_conv1d_silu with f32 x and y. */
+GLA_API int gla_conv1d_silu_f32(const float *x, const float *weight, const float *bias, const float *state_in,
+                                float *state_out, float *y, int B, int T, int D, const int32_t *cu_seqlens,
+                                void *stream);
+
+/*
+ * gla_conv1d_silu_step — the same operation for one new token of N sequences,
+ * in place on their conv states (decode):
+ *     y[n] = SiLU(bias + w0 s0 + w1 s1 + w2 s2 + w3 x[n]);  state[n] <- (s1, s2, x[n])
+ *   x, y [N, D] bf16;  state_inout [N, D, 3] f32;  weight, bias as above.
+ */
+GLA_API int gla_conv1d_silu_step(const void *x, const float *weight, const float *bias, float *state_inout,
+                                 void *y, int N, int D, void *stream);
+
+/*
  * gla_last_device_status — synchronise `stream`, then return and clear the
  * device status word: GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_DEVICE_ARG for the
  * first failure recorded by any kernel of this library on the current device

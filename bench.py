@@ -556,6 +556,43 @@ def run_e2e(args, P, D, w, wd, out, hT, dout, stream):
                     "the decode state stays resident on the device"}
 
 
+def run_only(args):
+    """W + K back-to-back calls of one operation (the backward of the layer workload, or the conv over
+    B8 T2048 D3072), then a device-status check: a fixed command line to put under a profiler."""
+    import torch
+    from gated_linear_rnn_gb300 import build as Bld
+    from gated_linear_rnn_gb300 import gla
+    from gated_linear_rnn_gb300 import inputs as I
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    Bld.build_library()
+    gla.load()
+    w = I.WORKLOADS["layer_bf16"]
+    if args.only == "backward":
+        d = I.make_backward(w, device=dev, seed=0, dhT_std=0.0)
+        dq, dk, dv = (torch.empty_like(d[k]) for k in ("q", "k", "v"))
+
+        def call():
+            gla.gla_chunk_bwd(d["q"], d["k"], d["v"], d["dout"], d["log_decay"], None, None, dq, dk, dv, None, w.chunk)
+    else:
+        g = torch.Generator(device=dev).manual_seed(11)
+        x = torch.randn(w.B, w.T, 3072, generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty_like(x)
+        wt = torch.randn(3072, 4, generator=g, device=dev) * 0.5
+        bias = torch.randn(3072, generator=g, device=dev) * 0.1
+
+        def call():
+            gla.gla_conv1d_silu(x, wt, bias, None, None, y)
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    st_code = gla.gla_last_device_status()
+    print(json.dumps({"only": args.only, "calls": args.warmup + args.steps, "status": st_code}), flush=True)
+    return 0 if st_code == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -564,10 +601,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-steps", type=int, default=5, help="timed launches of the backward (0: skip)")
+    ap.add_argument("--only", choices=["backward", "conv"], default=None,
+                    help="run just W + K calls of one operation on its bench workload (for profilers); "
+                         "prints one status line, not the bench line")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of fp64 reference work to time")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.only is not None:
+        return run_only(args)
     if args.impl == "reference":
         # the CPU reference arm: rank 0 alone works, no process group is needed
         world, rank, _ = dist_setup(init=False)

@@ -133,7 +133,11 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 // K/V stage (KPREP: the K rows of chunk c+1 may be ready before the MMA warp has waited for chunk c's);
 // with parity waits, a barrier must never run two phases ahead of a waiter.
 enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP0, B_KPREP1, B_SREADY,
-       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_COUNT };
+       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_COUNT };
+// barrier of K/V stage s (a state-only pass runs three stages, every other pass two)
+__device__ __forceinline__ int b_kvfull(int s) { return s == 0 ? B_KVFULL0 : s == 1 ? B_KVFULL1 : B_KVFULL2; }
+__device__ __forceinline__ int b_kvempty(int s) { return s == 0 ? B_KVEMPTY0 : s == 1 ? B_KVEMPTY1 : B_KVEMPTY2; }
+__device__ __forceinline__ int b_kprep(int s) { return s == 0 ? B_KPREP0 : s == 1 ? B_KPREP1 : B_KPREP2; }
 static_assert(B_COUNT <= 24, "the shared-memory plan reserves 24 barrier slots");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -167,8 +171,10 @@ __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, fl
 }
 
 // kRev: the reversed state pass of the backward (kStates with reverse set); a separate instantiation
-// so that the forward's register allocation is untouched.
-template <bool kRev>
+// so that the forward's register allocation is untouched.  kNst: K/V stages in flight; the forward's
+// state-only pass has three (its third K tile takes the unused Q buffer, its third V tile the unused
+// state-copy and output-staging space), every other pass two.
+template <bool kRev, int kNst>
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -227,6 +233,17 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // (lambda >= e^-0.3); stronger decays take the direct form: Q rows scaled by lambda^(i+1), K rows
     // by lambda^(L-1-j), per-element decay in the mask, state pre-scaled by lambda^L.
     const bool fact = ld >= -0.3f;
+    // The forward's state-only pass with a factored decay keeps the state in a frame that moves only
+    // every nblk chunks: within a block the K rows of its m-th chunk carry lambda^-(m*128 + j + 1), so
+    // the MMAs of consecutive chunks accumulate without a state pass between them, and at the block
+    // end one pass scales the state by lambda^(rows of the block).  nblk keeps every frame factor
+    // below e^36 (the latest rows, whose weight in the result is about 1, carry the largest).
+    const bool blocked = P.mode == kStateOnly && fact;
+    int nblk = 1;
+    if (blocked) {
+        const float a = -ld * (float)kC;  // >= 0
+        nblk = (a > 0.f) ? (int)fminf(64.f, fmaxf(1.f, floorf(36.f / a))) : 64;
+    }
     auto chunk_len = [&](int c) -> int {
         const int64_t rem = len - (int64_t)c * kC;
         return (int)(rem < kC ? rem : kC);
@@ -234,6 +251,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // the c-th chunk walked (backwards in time for a reversed state pass) and its length
     auto nat = [&](int c) -> int { return rev ? nchunks - 1 - c : c; };
     auto plen = [&](int c) -> int { return chunk_len(nat(c)); };
+    auto stg = [&](int c) -> int { return c % kNst; };          // K/V stage of the c-th chunk walked
+    auto sph = [&](int c) -> uint32_t { return (uint32_t)(c / kNst) & 1u; };  // its phase on that stage
+    auto kbuf_of = [&](int s) -> uint32_t { return s == 0 ? o_k0 : s == 1 ? o_k1 : o_q; };
+    auto vbuf_of = [&](int s) -> uint32_t { return s == 0 ? o_v0 : s == 1 ? o_v1 : o_s; };
 
     if (threadIdx.x == 0) {
         if (!valid) record_status(GLA_ERR_DEVICE_ARG);
@@ -254,6 +275,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_OFREE), 4);
         mbar_init(BAR(B_SFULL), 1);
         mbar_init(BAR(B_FINAL), 1);
+        mbar_init(BAR(B_KVFULL2), 1);
+        mbar_init(BAR(B_KVEMPTY2), 1);
+        mbar_init(BAR(B_KPREP2), 4);
         fence_mbar_init();
     }
     if (threadIdx.x < kC + 4) tab[threadIdx.x] = (threadIdx.x <= kC) ? expf((float)threadIdx.x * ld) : 0.f;
@@ -280,14 +304,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint32_t qbytes = (uint32_t)nka * 8192u;
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
-                const int s = c & 1;
+                const int s = stg(c);
                 const int y = row0 + nat(c) * kC;
-                if (c >= 2) ok = mbar_wait(BAR(B_KVEMPTY0 + s), ((c >> 1) - 1) & 1, abort_flag, kWaitBudgetNs);
+                if (c >= kNst) ok = mbar_wait(BAR(b_kvempty(s)), ((c / kNst) - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
-                mbar_expect_tx(BAR(B_KVFULL0 + s), kvbytes);
-                const uint32_t kdst = sbase + (s ? o_k1 : o_k0), vdst = sbase + (s ? o_v1 : o_v0);
-                for (int a = 0; a < nka; ++a) tma_load_2d(kdst + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(B_KVFULL0 + s));
-                for (int a = 0; a < nva; ++a) tma_load_2d(vdst + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(B_KVFULL0 + s));
+                mbar_expect_tx(BAR(b_kvfull(s)), kvbytes);
+                const uint32_t kdst = sbase + kbuf_of(s), vdst = sbase + vbuf_of(s);
+                for (int a = 0; a < nka; ++a) tma_load_2d(kdst + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(b_kvfull(s)));
+                for (int a = 0; a < nva; ++a) tma_load_2d(vdst + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(b_kvfull(s)));
                 if (!state_only) {
                     if (c >= 1) ok = mbar_wait(BAR(B_QEMPTY), (c - 1) & 1, abort_flag, kWaitBudgetNs);
                     if (!ok) break;
@@ -315,12 +339,29 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 write_images ? P.chunk_states + ((rng.start / kC + seq) * H + h) * sz_state : nullptr;
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
-                const int s = c & 1;
-                const uint32_t kbuf = sbase + (s ? o_k1 : o_k0), vbuf = sbase + (s ? o_v1 : o_v0);
+                const int s = stg(c);
+                const uint32_t kbuf = sbase + kbuf_of(s), vbuf = sbase + vbuf_of(s);
+                if (blocked) {
+                    // pass 1 in frame blocks: a state pass only before the first chunk of each block
+                    const int m = c % nblk;
+                    const bool block_end = (m == nblk - 1) || (c == nchunks - 1);
+                    ok = mbar_wait(BAR(b_kvfull(s)), sph(c), abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(b_kprep(s)), sph(c), abort_flag, kWaitBudgetNs) &&
+                         (m != 0 || mbar_wait(BAR(B_SREADY), (c / nblk) & 1, abort_flag, kWaitBudgetNs));
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < kC / 16; ++kk) {
+                        mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
+                               smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
+                    }
+                    mma_commit(BAR(b_kvempty(s)));
+                    if (block_end) mma_commit(BAR(B_SFULL));
+                    continue;
+                }
                 if (state_only) {
                     // pass 1: only the state chain, S += K~^T V per chunk
-                    ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
-                         mbar_wait(BAR(B_KPREP0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
+                    ok = mbar_wait(BAR(b_kvfull(s)), sph(c), abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(b_kprep(s)), sph(c), abort_flag, kWaitBudgetNs) &&
                          mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);
                     if (!ok) break;
                     tc_fence_after();
@@ -337,7 +378,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
                     }
                     mma_commit(BAR(B_SFULL));
-                    mma_commit(BAR(B_KVEMPTY0 + s));
+                    mma_commit(BAR(b_kvempty(s)));
                     continue;
                 }
                 ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
@@ -403,19 +444,92 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // Rows beyond the chunk are zeroed.
         const bool early_k = fact || state_only;
         auto prep_k_early = [&](int c) -> bool {
-            if (!mbar_wait(BAR(B_KVFULL0 + (c & 1)), (c >> 1) & 1, abort_flag, kWaitBudgetNs)) return false;
+            if (!mbar_wait(BAR(b_kvfull(stg(c))), sph(c), abort_flag, kWaitBudgetNs)) return false;
             const int Lk = plen(c);
             // forwards: lambda^-(j+1) (factored) or lambda^(L-1-j); backwards in time the weight of row i
             // is lambda^(i+1): lambda^(i+1-L) in the factored form (the state is scaled by lambda^L after)
             const float fw = fact ? utab[r] : tab[Lk - 1 - r];
             const float bw = fact ? tab[min(r + 1, kC)] * utab[Lk - 1] : tab[min(r + 1, kC)];
             const float f = (r < Lk) ? (rev ? bw : fw) : 0.f;
-            scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, f);
+            scale_row_sw64(smem + kbuf_of(stg(c)), nka, r, f);
             fence_async_shared();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_KPREP0 + (c & 1)));
+            if (lane == 0) mbar_arrive(BAR(b_kprep(stg(c))));
             return true;
         };
+        if (blocked) {
+            // K rows of chunk c (m-th of its block): lambda^-(m*128 + j + 1) k_j, rows beyond it zeroed
+            auto prep_k_frame = [&](int c) -> bool {
+                if (!mbar_wait(BAR(b_kvfull(stg(c))), sph(c), abort_flag, kWaitBudgetNs)) return false;
+                const int Lk = plen(c);
+                const float frame = expf(-ld * (float)((c % nblk) * kC));
+                scale_row_sw64(smem + kbuf_of(stg(c)), nka, r, (r < Lk) ? utab[r] * frame : 0.f);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(b_kprep(stg(c))));
+                return true;
+            };
+            // the starting state into TMEM
+            if (r < dk) {
+                for (int j0 = 0; j0 < dv; j0 += 32) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        v[e] = __float_as_uint(init_state ? __ldg(init_state + (int64_t)r * dv + j0 + e) : 0.f);
+                    tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SREADY));
+            if (nchunks > 0) ok = prep_k_frame(0);
+            for (int c = 0; c < nchunks && ok; ++c) {
+                if (c + 1 < nchunks) ok = prep_k_frame(c + 1);
+                if (!ok) break;
+                const int m = c % nblk;
+                if (m != nblk - 1 && c != nchunks - 1) continue;
+                // block end: S = lambda^(rows of the block) * (TMEM frame)
+                ok = mbar_wait(BAR(B_SFULL), (c / nblk) & 1, abort_flag, kWaitBudgetNs);
+                if (!ok) break;
+                tc_fence_after();
+                const bool last = c == nchunks - 1;
+                const float g = expf(ld * (float)(m * kC + plen(c)));
+                if (r < dk) {
+                    for (int j0 = 0; j0 < dv; j0 += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * g);
+                        if (last) {
+                            if (final_state) {
+                                float4 *dst = reinterpret_cast<float4 *>(final_state + (int64_t)r * dv + j0);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                            }
+                        } else {
+                            tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v);
+                        }
+                    }
+                }
+                if (!last) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(B_SREADY));
+                }
+            }
+            if (nchunks == 0 && final_state && r < dk) {
+                for (int j = 0; j < dv; ++j) final_state[(int64_t)r * dv + j] = init_state ? init_state[(int64_t)r * dv + j] : 0.f;
+            }
+            if (!ok) {
+                record_status(GLA_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        } else {
         if (early_k && nchunks > 0) ok = prep_k_early(0);
         for (int c = 0; c <= nchunks && ok; ++c) {
             if (c >= 1) {
@@ -517,6 +631,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             record_status(GLA_ERR_TIMEOUT);
             *abort_flag = 1;
         }
+        }  // not blocked
     } else if (warp < 8) {
         // ------------------------------------------------------------ mask warpgroup
         const int r = threadIdx.x - 128;                    // TMEM lane = token row
@@ -761,17 +876,29 @@ int plan_segments(int nseq, int H, int Tlen, const int32_t *cu, int *seg_chunks)
     return (nck + *seg_chunks - 1) / *seg_chunks;
 }
 
+// A third K/V stage takes the Q buffer (same size as a K tile) and the state copy plus the output
+// staging space for its V tile.
+bool three_stages_fit(int dk, int dv) {
+    const Smem p = smem_plan(dk, dv);
+    return (uint32_t)(dv / 64) * 16384u <= p.tab - p.s;
+}
+
 int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
               const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     if (p.reverse) {
-        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return GLA_ERR_LAUNCH;
-        gla_tc_chunk_kernel<true><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+        gla_tc_chunk_kernel<true, 2><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    } else if (p.mode == kStateOnly && three_stages_fit(p.dk, p.dv)) {
+        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes) != cudaSuccess)
+            return GLA_ERR_LAUNCH;
+        gla_tc_chunk_kernel<false, 3><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
     } else {
-        gla_tc_chunk_kernel<false><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+        gla_tc_chunk_kernel<false, 2><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
     }
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
@@ -792,7 +919,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
         return GLA_ERR_LAUNCH;
     const Smem sp = smem_plan(dk, dv);
     const size_t bytes = sp.total + 1024;  // + alignment slack
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
         return GLA_ERR_LAUNCH;
     Params p{};
@@ -864,7 +991,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
         !make_map(&mv, va, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
     const size_t bytes = smem_plan(dk, dv).total + 1024;
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
         return GLA_ERR_LAUNCH;
     Params p{};
@@ -943,7 +1070,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
         !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
         return GLA_ERR_LAUNCH;
     const size_t bytes = smem_plan(dk, dv).total + 1024;
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
         cudaSuccess)
         return GLA_ERR_LAUNCH;
     Params p{};

@@ -133,7 +133,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 // K/V stage (KPREP: the K rows of chunk c+1 may be ready before the MMA warp has waited for chunk c's);
 // with parity waits, a barrier must never run two phases ahead of a waiter.
 enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP0, B_KPREP1, B_SREADY,
-       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_COUNT };
+       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_IMGDONE, B_COUNT };
 // barrier of K/V stage s (a state-only pass runs three stages, every other pass two)
 __device__ __forceinline__ int b_kvfull(int s) { return s == 0 ? B_KVFULL0 : s == 1 ? B_KVFULL1 : B_KVFULL2; }
 __device__ __forceinline__ int b_kvempty(int s) { return s == 0 ? B_KVEMPTY0 : s == 1 ? B_KVEMPTY1 : B_KVEMPTY2; }
@@ -239,8 +239,16 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // end one pass scales the state by lambda^(rows of the block).  nblk keeps every frame factor
     // below e^36 (the latest rows, whose weight in the result is about 1, carry the largest).
     const bool blocked = P.mode == kStateOnly && fact;
+    // The backward's state passes (kStates) with a factored decay use the same moving frame; the
+    // state before each chunk, for its image, is lambda^(rows walked in the block so far) times the
+    // frame, so only the block ends write the state back to TMEM, and the image's copy out of shared
+    // memory runs while the next MMA does.
+    const bool framed = P.mode == kStates && fact;
+    // The backward does not use the state passes' results for strong decays (the chunked SIMT
+    // recurrences own those heads, dh0 included), so their CTAs have nothing to do.
+    if (P.mode == kStates && !fact) return;
     int nblk = 1;
-    if (blocked) {
+    if (blocked || framed) {
         const float a = -ld * (float)kC;  // >= 0
         nblk = (a > 0.f) ? (int)fminf(64.f, fmaxf(1.f, floorf(36.f / a))) : 64;
     }
@@ -278,6 +286,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_KVFULL2), 1);
         mbar_init(BAR(B_KVEMPTY2), 1);
         mbar_init(BAR(B_KPREP2), 4);
+        mbar_init(BAR(B_IMGDONE), 1);
         fence_mbar_init();
     }
     if (threadIdx.x < kC + 4) tab[threadIdx.x] = (threadIdx.x <= kC) ? expf((float)threadIdx.x * ld) : 0.f;
@@ -341,6 +350,25 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = stg(c);
                 const uint32_t kbuf = sbase + kbuf_of(s), vbuf = sbase + vbuf_of(s);
+                if (framed) {
+                    ok = mbar_wait(BAR(b_kvfull(s)), sph(c), abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(b_kprep(s)), sph(c), abort_flag, kWaitBudgetNs) &&
+                         mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < kC / 16; ++kk) {
+                        mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
+                               smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
+                    }
+                    mma_commit(BAR(B_SFULL));
+                    mma_commit(BAR(b_kvempty(s)));
+                    // the image of the state before this chunk: copy it out while the MMA runs
+                    bulk_store_s2g(img0 + (int64_t)nat(c) * H * sz_state, sbase + o_s, (uint32_t)(sz_state * 2));
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(BAR(B_IMGDONE));
+                    continue;
+                }
                 if (blocked) {
                     // pass 1 in frame blocks: a state pass only before the first chunk of each block
                     const int m = c % nblk;
@@ -457,7 +485,102 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (lane == 0) mbar_arrive(BAR(b_kprep(stg(c))));
             return true;
         };
-        if (blocked) {
+        if (framed) {
+            // rows walked in the current frame block before the c-th chunk (only the first chunk walked
+            // backwards, the sequence's last, can be short; walked forwards the short one comes last)
+            auto rows_before = [&](int c) -> int {
+                const int m = c % nblk;
+                return m * kC - ((rev && c > 0 && c < nblk) ? (kC - plen(0)) : 0);
+            };
+            // K-role rows of the c-th chunk walked, with their frame factor; rows beyond it zeroed
+            auto prep_k_framed = [&](int c) -> bool {
+                if (!mbar_wait(BAR(b_kvfull(stg(c))), sph(c), abort_flag, kWaitBudgetNs)) return false;
+                const int Lk = plen(c);
+                const int e = rows_before(c) + (rev ? Lk - r - 1 : r + 1);
+                scale_row_sw64(smem + kbuf_of(stg(c)), nka, r, (r < Lk) ? expf(-ld * (float)e) : 0.f);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(b_kprep(stg(c))));
+                return true;
+            };
+            if (nchunks > 0) ok = prep_k_framed(0);
+            int walked = 0;  // rows walked in the current block before the c-th chunk
+            for (int c = 0; c <= nchunks && ok; ++c) {
+                const bool last = c == nchunks;
+                const bool block_start = c > 0 && (c % nblk == 0 || last);  // the previous block just ended
+                if (c >= 1) {
+                    ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                    // the previous image must be out of shared memory before the copy is refilled
+                    if (ok && !last) ok = mbar_wait(BAR(B_IMGDONE), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // state before the c-th chunk: lambda^walked * frame; at a block start the frame is
+                // brought back to the true state (TMEM rewritten) and walked restarts at 0
+                const float g = expf(ld * (float)walked);
+                if (r < dk) {
+                    for (int j0 = 0; j0 < dv; j0 += 64) {
+                        uint32_t v[2][32];
+                        if (c >= 1) {
+                            tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
+                            tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * g);
+                                v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                v[0][e] = __float_as_uint(init_state ? __ldg(init_state + (int64_t)r * dv + j0 + e) : 0.f);
+                                v[1][e] = __float_as_uint(init_state ? __ldg(init_state + (int64_t)r * dv + j0 + 32 + e) : 0.f);
+                            }
+                        }
+                        if (last) {
+                            if (final_state) {
+                                float4 *dst = reinterpret_cast<float4 *>(final_state + (int64_t)r * dv + j0);
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    dst[e] = make_float4(__uint_as_float(v[e >> 3][4 * (e & 7)]),
+                                                         __uint_as_float(v[e >> 3][4 * (e & 7) + 1]),
+                                                         __uint_as_float(v[e >> 3][4 * (e & 7) + 2]),
+                                                         __uint_as_float(v[e >> 3][4 * (e & 7) + 3]));
+                            }
+                            continue;
+                        }
+                        if (c == 0 || block_start) {
+                            tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
+                            tmem_st32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
+                        }
+                        // bf16 image into the MN-major, 128B-swizzled tile: one 64-column atom
+                        uint8_t *atom_row = smem + o_s + (uint32_t)(j0 >> 6) * (uint32_t)dk * 128u + (uint32_t)r * 128u;
+#pragma unroll
+                        for (int q8 = 0; q8 < 8; ++q8) {
+                            const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                            *reinterpret_cast<uint4 *>(atom_row + (((uint32_t)q8 ^ (uint32_t)(r & 7)) << 4)) =
+                                make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                           pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                           pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                           pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                        }
+                    }
+                }
+                if (last) break;
+                if (block_start) walked = 0;
+                tmem_wait_st();
+                fence_async_shared();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_SREADY));
+                walked += plen(c);
+                if (c + 1 < nchunks) ok = prep_k_framed(c + 1);
+            }
+            if (!ok) {
+                record_status(GLA_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        } else if (blocked) {
             // K rows of chunk c (m-th of its block): lambda^-(m*128 + j + 1) k_j, rows beyond it zeroed
             auto prep_k_frame = [&](int c) -> bool {
                 if (!mbar_wait(BAR(b_kvfull(stg(c))), sph(c), abort_flag, kWaitBudgetNs)) return false;
@@ -887,12 +1010,13 @@ int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &m
               const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
+    const bool three = p.mode == kStateOnly && three_stages_fit(p.dk, p.dv);
     if (p.reverse) {
         if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return GLA_ERR_LAUNCH;
         gla_tc_chunk_kernel<true, 2><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
-    } else if (p.mode == kStateOnly && three_stages_fit(p.dk, p.dv)) {
+    } else if (three) {
         if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return GLA_ERR_LAUNCH;

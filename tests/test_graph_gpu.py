@@ -1,0 +1,95 @@
+"""The library inside CUDA graphs and on concurrent streams.
+
+A serving or training loop captures its steps once and replays them.  These tests capture the
+chunked forward (whole-chain and segmented schedules), the backward and a decode step in one graph,
+replay it with new inputs copied into the captured buffers, and require results bit-identical to
+eager calls on the same inputs (the kernels are deterministic).  A second test runs two forwards on
+two streams at once and checks each against its eager result.
+"""
+import pytest
+import torch
+
+from gated_linear_rnn_gb300 import build as B
+from gated_linear_rnn_gb300 import gla
+from gated_linear_rnn_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    B.build_library()
+    gla.load()
+    torch.cuda.set_device(0)
+    yield
+    assert gla.gla_last_device_status() == 0
+
+
+def eager(d, w, dd):
+    out, hT = gla.chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], chunk=128)
+    grads = gla.chunk_bwd(d["q"], d["k"], d["v"], d["dout"], d["log_decay"], d["h0"], d["dhT"], chunk=128)
+    st = dd["state"].clone()
+    o = gla.decode_step(dd["q"], dd["k"], dd["v"], dd["log_decay"], st)
+    torch.cuda.synchronize()
+    return [out, hT, *grads, o, st]
+
+
+@pytest.mark.parametrize("B_,T", [(2, 640), (1, 4096)])  # whole-chain schedule; segmented (few long chains)
+def test_graph_replay_matches_eager(B_, T):
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=B_, T=T, H=4, h0_std=0.02)
+    wd = I.scaled(I.WORKLOADS["decode"], B=16)
+    bufs = I.make_backward(w, device="cuda", seed=1)
+    dbufs = I.make_decode(wd, device="cuda", seed=1)
+    state = dbufs["state"].clone()
+    out = torch.empty(bufs["q"].shape[:3] + (w.dv,), dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty(B_, w.H, w.dk, w.dv, device="cuda")
+    dq, dk, dv = (torch.empty_like(bufs[k]) for k in ("q", "k", "v"))
+    dh0 = torch.empty_like(hT)
+    dout_dec = torch.empty(16, wd.H, wd.dv, dtype=torch.bfloat16, device="cuda")
+
+    def step(stream=None):
+        gla.gla_chunk_fwd(bufs["q"], bufs["k"], bufs["v"], bufs["log_decay"], bufs["h0"], out, hT, 128, None, stream)
+        gla.gla_chunk_bwd(bufs["q"], bufs["k"], bufs["v"], bufs["dout"], bufs["log_decay"], bufs["h0"], bufs["dhT"],
+                          dq, dk, dv, dh0, 128, None, stream)
+        gla.gla_decode_step(dbufs["q"], dbufs["k"], dbufs["v"], dbufs["log_decay"], state, dout_dec, stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(s)  # warm-up outside the capture (first-call lookups)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in (5, 6):
+        d = I.make_backward(w, device="cuda", seed=seed)
+        dd = I.make_decode(wd, device="cuda", seed=seed)
+        for k in ("q", "k", "v", "dout", "h0", "dhT"):
+            bufs[k].copy_(d[k])
+        for k in ("q", "k", "v"):
+            dbufs[k].copy_(dd[k])
+        state.copy_(dd["state"])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gla.gla_last_device_status() == 0
+        ref = eager(d, w, dd)
+        got = [out, hT, dq, dk, dv, dh0, dout_dec, state]
+        for name, g, r in zip(("out", "hT", "dq", "dk", "dv", "dh0", "decode out", "decode state"), got, ref):
+            assert torch.equal(g, r), f"{name} differs after replay (seed {seed})"
+
+
+def test_two_streams_at_once():
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=4, T=1024, H=8, h0_std=0.02)
+    ds = [I.make_prefill(w, device="cuda", seed=s) for s in (11, 12)]
+    refs = [gla.chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], chunk=128) for d in ds]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for d, st in zip(ds, streams):
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            outs.append(gla.chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], chunk=128, stream=st))
+    torch.cuda.synchronize()
+    for (o, h), (ro, rh) in zip(outs, refs):
+        assert torch.equal(o, ro) and torch.equal(h, rh)

@@ -196,17 +196,21 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + plan.abort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chain = blockIdx.x / P.grid_seg, seg = blockIdx.x % P.grid_seg;
+    constexpr bool rev = kRev;
+    // segment w in walk order of this CTA's chain; walked backwards in time, walk order runs from the
+    // sequence's last segment to its first
+    const int chain = blockIdx.x / P.grid_seg, w = blockIdx.x % P.grid_seg;
+    const int seg = rev ? P.nseg - 1 - w : w;  // natural segment
     const int seq = chain / H, h = chain % H;
     const bool state_only = P.mode == kStateOnly || P.mode == kStates;
-    constexpr bool rev = kRev;
     const bool write_images = P.mode == kStates && P.chunk_states != nullptr;
+    const bool segmented = P.mode == kStateOnly || P.mode == kSegmented || (P.mode == kStates && P.nseg > 1);
 
     SeqRange rng;
     const bool valid = seq_range(seq, P.T, P.cu, rng);
     int64_t len = valid ? rng.len : 0;
     int64_t start = rng.start;
-    if (P.mode == kStateOnly || P.mode == kSegmented) {  // one segment of a dense sequence
+    if (segmented) {  // one segment of a dense sequence
         const int64_t s0 = (int64_t)seg * P.seg_chunks * kC;
         start += s0;
         len = (len - s0 < (int64_t)P.seg_chunks * kC) ? len - s0 : (int64_t)P.seg_chunks * kC;
@@ -217,12 +221,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int64_t sz_state = (int64_t)P.dk * P.dv;
     const float *init_state = P.h0 ? P.h0 + ((int64_t)seq * H + h) * sz_state : nullptr;
     float *final_state = P.hT ? P.hT + ((int64_t)seq * H + h) * sz_state : nullptr;
+    // per chain, segment scratch is [nseg - 1] states in walk order: the end states from zero of walk
+    // segments 0..nseg-2 (pass 1), and the start states of walk segments 1..nseg-1 (after the scan)
     if (P.mode == kStateOnly) {
         init_state = nullptr;
-        final_state = P.seg_end + ((int64_t)chain * (P.nseg - 1) + seg) * sz_state;
-    } else if (P.mode == kSegmented) {
-        if (seg > 0) init_state = P.seg_h0 + ((int64_t)chain * (P.nseg - 1) + seg - 1) * sz_state;
-        if (seg < P.nseg - 1) final_state = nullptr;
+        final_state = P.seg_end + ((int64_t)chain * (P.nseg - 1) + w) * sz_state;
+    } else if (segmented) {
+        if (w > 0) init_state = P.seg_h0 + ((int64_t)chain * (P.nseg - 1) + w - 1) * sz_state;
+        if (w < P.nseg - 1) final_state = nullptr;
     }
     const float ld = __ldg(P.log_decay + h);
     const float lam = expf(ld);
@@ -344,8 +350,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const int ksteps_dk = dk / 16;
             const uint32_t qbuf = sbase + o_q, sbuf = sbase + o_s;
             // image of the state before chunk 0 of this chain (slot start / 128 + seq; chunk c adds c slots)
-            __nv_bfloat16 *const img0 =
-                write_images ? P.chunk_states + ((rng.start / kC + seq) * H + h) * sz_state : nullptr;
+            // image slot of the state before this segment's first chunk (sequence slot start / 128 + seq,
+            // plus the segment's first chunk)
+            __nv_bfloat16 *img0 = nullptr;
+            if (write_images) {
+                const int ws = blockIdx.x % P.grid_seg;
+                const int64_t first_chunk = P.nseg > 1 ? (int64_t)(rev ? P.nseg - 1 - ws : ws) * P.seg_chunks : 0;
+                img0 = P.chunk_states + ((rng.start / kC + seq + first_chunk) * H + h) * sz_state;
+            }
             bool ok = true;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int s = stg(c);
@@ -582,11 +594,21 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         } else if (blocked) {
             // K rows of chunk c (m-th of its block): lambda^-(m*128 + j + 1) k_j, rows beyond it zeroed
+            // rows walked in the current frame block before the c-th chunk (walked backwards only the
+            // first chunk, the sequence's last, can be short; walked forwards the short one comes last)
+            auto rows_before = [&](int c) -> int {
+                return (c % nblk) * kC - ((rev && c > 0 && c < nblk) ? (kC - plen(0)) : 0);
+            };
             auto prep_k_frame = [&](int c) -> bool {
                 if (!mbar_wait(BAR(b_kvfull(stg(c))), sph(c), abort_flag, kWaitBudgetNs)) return false;
                 const int Lk = plen(c);
-                const float frame = expf(-ld * (float)((c % nblk) * kC));
-                scale_row_sw64(smem + kbuf_of(stg(c)), nka, r, (r < Lk) ? utab[r] * frame : 0.f);
+                float f;
+                if (rev) {  // row i of a chunk walked backwards: lambda^-(rows before it in the block + L - i - 1)
+                    f = expf(-ld * (float)(rows_before(c) + Lk - r - 1));
+                } else {    // row j walked forwards: lambda^-(128 m + j + 1)
+                    f = utab[r] * expf(-ld * (float)((c % nblk) * kC));
+                }
+                scale_row_sw64(smem + kbuf_of(stg(c)), nka, r, (r < Lk) ? f : 0.f);
                 fence_async_shared();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(b_kprep(stg(c))));
@@ -617,7 +639,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 const bool last = c == nchunks - 1;
-                const float g = expf(ld * (float)(m * kC + plen(c)));
+                const float g = expf(ld * (float)(rows_before(c) + plen(c)));
                 if (r < dk) {
                     for (int j0 = 0; j0 < dv; j0 += 32) {
                         uint32_t v[32];
@@ -913,14 +935,16 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 __global__ void __launch_bounds__(256)
 gla_seg_scan_kernel(const float *__restrict__ log_decay, const float *__restrict__ h0,
                     const float *__restrict__ seg_end, float *__restrict__ seg_h0, int H, int dk, int dv,
-                    int nseg, int seg_tokens) {
+                    int nseg, int seg_tokens, int first_tokens) {
     const int chain = blockIdx.y, h = chain % H;
     const int64_t sz = (int64_t)dk * dv;
     const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e >= sz) return;
     float4 S = h0 ? __ldg(reinterpret_cast<const float4 *>(h0 + chain * sz + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float g = expf(__ldg(log_decay + h) * (float)seg_tokens);
+    const float ld = __ldg(log_decay + h);
     for (int s = 0; s + 1 < nseg; ++s) {
+        // walk segment s has seg_tokens rows, except the first walked backwards (first_tokens)
+        const float g = expf(ld * (float)(s == 0 ? first_tokens : seg_tokens));
         const int64_t off = ((int64_t)chain * (nseg - 1) + s) * sz + e;
         const float4 E = __ldg(reinterpret_cast<const float4 *>(seg_end + off));
         S.x = fmaf(g, S.x, E.x);
@@ -1011,7 +1035,12 @@ int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &m
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     const bool three = p.mode == kStateOnly && three_stages_fit(p.dk, p.dv);
-    if (p.reverse) {
+    if (p.reverse && three) {
+        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes) != cudaSuccess)
+            return GLA_ERR_LAUNCH;
+        gla_tc_chunk_kernel<true, 3><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    } else if (p.reverse) {
         if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess)
             return GLA_ERR_LAUNCH;
@@ -1084,7 +1113,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (rc == GLA_OK) {
         dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
         gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg,
-                                                  seg_chunks * kC);
+                                                  seg_chunks * kC, seg_chunks * kC);
         count_launches(1);
         rc = cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
     }
@@ -1132,8 +1161,44 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     p.grid_seg = 1;
     p.reverse = reverse ? 1 : 0;
     p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
+    const long long chains = (long long)nseq * H;
+    int seg_chunks = 0;
+    const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
     // the q and out maps are not read in a state-only pass
-    return launch_tc(mk, mk, mv, mv, p, (long long)nseq * H, bytes, st);
+    if (nseg == 1) return launch_tc(mk, mk, mv, mv, p, chains, bytes, st);
+
+    // few long chains: as the forward's segmented schedule, in walk order (backwards in time the first
+    // walked segment is the sequence's last, which may be short): end states of walk segments
+    // 0..nseg-2 from zero, a scan for the start states, then every segment from its start state
+    const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
+    float *scratch = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), 2 * per * sizeof(float), st) != cudaSuccess) {
+        cudaGetLastError();
+        return GLA_ERR_NOMEM;
+    }
+    p.nseg = nseg;
+    p.seg_chunks = seg_chunks;
+    p.seg_end = scratch;
+    p.seg_h0 = scratch + per;
+    p.mode = kStateOnly;
+    p.grid_seg = nseg - 1;
+    int rc = launch_tc(mk, mk, mv, mv, p, chains * (nseg - 1), bytes, st);
+    if (rc == GLA_OK) {
+        const int seg_tokens = seg_chunks * kC;
+        const int first_tokens = reverse ? Tlen - (nseg - 1) * seg_tokens : seg_tokens;
+        dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
+        gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, init, p.seg_end, scratch + per, H, dk, dv, nseg, seg_tokens,
+                                                  first_tokens);
+        count_launches(1);
+        rc = cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
+    }
+    if (rc == GLA_OK) {
+        p.mode = kStates;
+        p.grid_seg = nseg;
+        rc = launch_tc(mk, mk, mv, mv, p, chains * nseg, bytes, st);
+    }
+    cudaFreeAsync(scratch, st);
+    return rc;
 }
 
 // ---- no-alloc variant ------------------------------------------------------------
@@ -1216,7 +1281,8 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
     if (rc != GLA_OK) return rc;
     dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
-    gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC);
+    gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC,
+                                              seg_chunks * kC);
     count_launches(1);
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     p.mode = kSegmented;

@@ -121,3 +121,12 @@ def test_backward_matches_forward_linearisation():
     lhs = float(np.sum(dq.astype(np.float64) * d["q"].float().cpu().numpy()))
     rhs = float(np.sum(d["dout"].float().cpu().numpy().astype(np.float64) * out.float().cpu().numpy()))
     assert abs(lhs - rhs) <= 2e-2 * max(1.0, abs(rhs))
+
+
+@pytest.mark.parametrize("T,H,lo,hi", [(4096, 2, 1 / 32, 1 / 4096), (4000, 3, 1 / 32, 1 / 4096), (3000, 2, 0.6, 1 / 4096)])
+def test_backward_segmented_state_passes(T, H, lo, hi):
+    """Few long chains: both state passes run segmented (segment end states from zero, a scan, then
+    every segment from its start state); T = 4000 leaves a short last segment and a partial last
+    chunk, the last case mixes heads the SIMT recurrences own."""
+    w = I.scaled(I.WORKLOADS["long_bf16"], B=1, T=T, H=H, h0_std=0.02, decay_lo=lo, decay_hi=hi)
+    check_backward(w, seed=T)

@@ -41,6 +41,8 @@ int conv1d_silu_bf16(const void *, const float *, const float *, const float *, 
 int conv1d_silu_f32(const float *, const float *, const float *, const float *, float *, float *, int, int, int,
                     const int32_t *, cudaStream_t);
 int conv1d_silu_step_bf16(const void *, const float *, const float *, float *, void *, int, int, cudaStream_t);
+int chunk_fwd_host_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *,
+                        int, int, int, int, int, int, cudaStream_t);
 int take_status_conv(cudaStream_t);
 int take_status_simt(cudaStream_t);
 int take_status_bwd(cudaStream_t);
@@ -158,6 +160,19 @@ int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
         return tc_chunk_fwd_bf16_noalloc(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens, st);
     // the SIMT kernel takes no scratch
     return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
+}
+
+int gla_chunk_fwd_host(const void *q, const void *k, const void *v, const float *log_decay, const float *h0,
+                       void *out, float *hT, int B, int T, int H, int dk, int dv, int chunk, void *stream) {
+    // host pointers: the alignment rules of device buffers do not apply (the copies take any address)
+    if (!q || !k || !v || !out) return GLA_ERR_ARG;
+    int rc = check_decays_and_sizes(log_decay, B, T, H, dk, dv);
+    if (rc) return rc;
+    if (dk < 16 || dk > 256 || dv < 16 || dv > 512 || dk % 8 || dv % 8) return GLA_ERR_UNSUPPORTED;
+    if ((long long)B * T * H > (1LL << 40)) return GLA_ERR_UNSUPPORTED;
+    if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return GLA_ERR_UNSUPPORTED;
+    if (!device_info().ok) return GLA_ERR_UNSUPPORTED;
+    return chunk_fwd_host_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, (cudaStream_t)stream);
 }
 
 int gla_chunk_fwd_f32(const float *q, const float *k, const float *v, const float *log_decay, const float *h0,

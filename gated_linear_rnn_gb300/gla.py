@@ -28,6 +28,7 @@ _P, _I = ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "gla_chunk_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_fwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_fwd_host": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_bwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
@@ -149,6 +150,31 @@ def gla_chunk_fwd_noalloc(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlen
     rc = load().gla_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
                                       nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens), _stream(stream))
     _raise(rc, "gla_chunk_fwd_noalloc")
+
+
+def gla_chunk_fwd_host(q, k, v, log_decay, h0, out, hT, chunk: int, stream=None) -> None:
+    """bf16 chunked forward on HOST tensors (pinned for overlap): copies in, computes and copies out
+    in groups of sequences on three streams.  Enqueues and returns; the results are in ``out`` / ``hT``
+    once ``stream`` has reached the call.  See include/gla.h."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, dk]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, name, dtype, shape in ((q, "q", torch.bfloat16, None), (k, "k", torch.bfloat16, (B, T, H, dk)),
+                                  (v, "v", torch.bfloat16, (B, T, H, dv)), (out, "out", torch.bfloat16, (B, T, H, dv)),
+                                  (log_decay, "log_decay", torch.float32, (H,)),
+                                  (h0, "h0", torch.float32, (B, H, dk, dv)), (hT, "hT", torch.float32, (B, H, dk, dv))):
+        if t is None:
+            if name in ("h0", "hT"):
+                continue
+            raise ValueError(f"{name} is required")
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+        if t.dtype != dtype or not t.is_contiguous() or (shape is not None and tuple(t.shape) != tuple(shape)):
+            raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape or '[B, T, H, dk]'}")
+    rc = load().gla_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
+                                   B, T, H, dk, dv, int(chunk), _stream(stream))
+    _raise(rc, "gla_chunk_fwd_host")
 
 
 def gla_chunk_fwd_f32(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, stream=None) -> None:

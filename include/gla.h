@@ -17,7 +17,8 @@
  * Conventions shared by every entry point
  *   - Layouts are row-major with the innermost dimension last.
  *   - Every pointer argument is a DEVICE pointer of the current CUDA device and
- *     must be 16-byte aligned (GLA_ERR_ALIGN otherwise).  The caller owns every
+ *     must be 16-byte aligned (GLA_ERR_ALIGN otherwise); gla_chunk_fwd_host
+ *     alone takes host pointers, with no alignment rule.  The caller owns every
  *     buffer; the library never frees or keeps a caller pointer.
  *   - "bf16" means IEEE-754 binary16-bfloat (torch.bfloat16); "f32" float.
  *     States (h0, hT, state_inout) and log_decay are always f32, and all
@@ -137,6 +138,44 @@ GLA_API int gla_chunk_fwd(const void *q, const void *k, const void *v, const flo
 GLA_API int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_decay,
                                   const float *h0, void *out, float *hT, int B, int T, int H, int dk,
                                   int dv, int chunk, const int32_t *cu_seqlens, void *stream);
+
+/*
+ * gla_chunk_fwd_host — gla_chunk_fwd on HOST arrays, with the copies overlapped.
+ *
+ * Computes the map of gla_chunk_fwd (same recurrence, same kernels) for a
+ * dense batch whose q, k, v, log_decay and h0 live in host memory, and writes
+ * out and hT to host memory.  The batch is cut into groups of whole sequences
+ * (at most 8 groups, none under 8 MiB of copies unless the batch is smaller);
+ * group g+1 is copied to the device while group g computes on `stream` and
+ * group g-1 is copied back on a third (the library's own), so the copies in
+ * both directions and the compute run at the same time.  A group's
+ * sequences are computed as a batch of their own, so results can differ from
+ * one gla_chunk_fwd call on the whole batch in the last bits (the schedule
+ * depends on the number of chains), never by more than rounding.
+ *
+ * Arguments are those of gla_chunk_fwd without cu_seqlens (packed batches are
+ * not taken here), with every array a HOST pointer in the same layout:
+ *   q, k [B, T, H, dk] bf16; v, out [B, T, H, dv] bf16; log_decay [H] f32;
+ *   h0, hT [B, H, dk, dv] f32 or NULL.
+ * Page-locked (pinned) host memory lets the copies run asynchronously and
+ * overlap; pageable memory works but the driver stages it and the overlap is
+ * lost.  No host alignment is required.
+ *
+ * Ownership: the arrays stay the caller's.  The call enqueues work and returns;
+ * out and hT are written, and the input arrays may be reused, once `stream`
+ * reaches the point of the call (cudaStreamSynchronize(stream) or an event
+ * recorded after the call).  Device scratch for two groups plus log_decay is
+ * taken with cudaMallocAsync on `stream` and freed in stream order.  The two
+ * copy streams are the library's own (per device, created on first use).
+ *
+ * Errors: GLA_ERR_ARG / GLA_ERR_UNSUPPORTED as gla_chunk_fwd (checked before
+ * anything is enqueued); GLA_ERR_NOMEM if the scratch cannot be allocated;
+ * GLA_ERR_LAUNCH if an enqueue fails (the call then waits for what it had
+ * enqueued before it frees the scratch).  Device-side status as gla_chunk_fwd.
+ */
+GLA_API int gla_chunk_fwd_host(const void *q, const void *k, const void *v, const float *log_decay,
+                               const float *h0, void *out, float *hT, int B, int T, int H, int dk, int dv,
+                               int chunk, void *stream);
 
 /* gla_chunk_fwd_f32 — as gla_chunk_fwd with f32 q, k, v and out.  Always runs
  * the SIMT kernel (f32 FMA, no tensor cores): chunk in {16, 32, 64, 128}.

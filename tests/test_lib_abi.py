@@ -82,3 +82,14 @@ def test_unsupported_shapes_and_alignment_rejected_on_the_host(lib):
     odd = P(4096 + 8)
     assert lib.gla_chunk_fwd(odd, fake, fake, fake, None, fake, None, 1, 8, 1, 16, 16, 128, None, None) == -3
     assert lib.gla_decode_step(fake, fake, fake, fake, odd, fake, 1, 1, 16, 16, None) == -3
+
+
+def test_host_entry_rejects_bad_arguments_before_any_copy(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    # null inputs, non-positive sizes, unsupported head sizes and chunk lengths
+    assert lib.gla_chunk_fwd_host(None, fake, fake, fake, None, fake, None, 1, 1, 1, 16, 16, 128, None) == -1
+    assert lib.gla_chunk_fwd_host(fake, fake, fake, None, None, fake, None, 1, 1, 1, 16, 16, 128, None) == -1
+    assert lib.gla_chunk_fwd_host(fake, fake, fake, fake, None, fake, None, 1, 0, 1, 16, 16, 128, None) == -1
+    assert lib.gla_chunk_fwd_host(fake, fake, fake, fake, None, fake, None, 1, 8, 1, 20, 64, 128, None) == -2
+    assert lib.gla_chunk_fwd_host(fake, fake, fake, fake, None, fake, None, 1, 8, 1, 64, 64, 48, None) == -2

@@ -11,22 +11,25 @@
 // three inputs, so a sequence can be continued in a later call or by the
 // per-token step below.
 //
-// Prefill: a thread owns 8 consecutive channels (one 16-byte bf16 vector) and
-// a run of 8 rows, all loaded at once, with the three inputs before its current
-// row in registers; a warp covers 256 channels = 512 contiguous bytes of a row.
-// The three rows before a run are read again by it (through L2), so HBM sees
-// every input about once and every output once (4 bytes per element for
-// bf16).  Step: one thread per 8 channels of one sequence.
+// Prefill: a TMA pipeline over 64-row tiles of a 256-channel slab (the box also
+// carries the three rows before the tile), a lane owning 8 channels of 8 rows
+// with the three inputs before its row in registers (details at the kernel).
+// HBM sees every input about once (the three extra rows per tile come from L2)
+// and every output once.  Step: one thread per 8 channels of one sequence.
+#include <cuda.h>
+
+#include <atomic>
+
 #include "gla_common.cuh"
+#include "sm100_ptx.cuh"
 
 GLA_DEFINE_STATUS(conv)
 
 namespace gla {
 namespace {
 
-constexpr int kThreads = 256;  // prefill: 8 runs x 256 channels per block; step: 2048 channels
+constexpr int kThreads = 256;  // step kernel: 2048 channels per block
 constexpr int kVec = 8;        // channels per thread
-constexpr int kRun = 8;        // rows per thread in the prefill kernel, all loaded before the first is used
 
 template <typename T>
 struct Vec8;
@@ -97,13 +100,11 @@ __device__ __forceinline__ float tanh_approx(float x) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// SiLU of the prefill kernel, whose argument comes scaled: z itself for f32, z / 2 for bf16 (the tanh form)
 template <typename T>
-__device__ __forceinline__ float silu_t(float z) { return silu(z); }
+__device__ __forceinline__ float silu_scaled(float z) { return silu(z); }
 template <>
-__device__ __forceinline__ float silu_t<__nv_bfloat16>(float z) {
-    const float hz = 0.5f * z;
-    return fmaf(hz, tanh_approx(hz), hz);
-}
+__device__ __forceinline__ float silu_scaled<__nv_bfloat16>(float hz) { return fmaf(hz, tanh_approx(hz), hz); }
 
 // sequence of `row` and its [start, end) rows; dense batches have cu == null
 __device__ __forceinline__ int seq_of(int64_t row, int nseq, int T, const int32_t *cu, int64_t &start,
@@ -127,80 +128,188 @@ __device__ __forceinline__ int seq_of(int64_t row, int nseq, int T, const int32_
     return s;
 }
 
+// Prefill pipeline.  A CTA owns a slab of up to 256 channels and walks 64-row tiles of it (tile t,
+// then t + gridDim.x, ...).  A producer warp brings each tile in with one TMA box that also holds the
+// three rows before the tile (rows from -3 are zero-filled), into a ring of shared-memory stages; eight
+// compute warps take 8 rows each: a lane owns 8 channels, keeps the three inputs before its row in
+// registers and stores its 16 bytes of y, so a warp writes whole 512-byte rows.  The bytes in flight
+// are the stages in shared memory, not registers.
+constexpr int kCvWarps = 8;                     // compute warps
+constexpr int kCvRun = 8;                       // rows per compute warp and tile
+constexpr int kCvTile = kCvWarps * kCvRun;      // 64 rows per tile
+constexpr int kCvBoxRows = kCvTile + 3;         // + the three rows before the tile
+constexpr int kCvThreads = (kCvWarps + 1) * 32; // + the producer warp
+constexpr int kCvSlab = 256;                    // channels per CTA (the TMA box is at most 256 wide)
+constexpr uint64_t kCvWaitNs = 2000000000ull;   // 2 s per wait
+
+template <typename T> struct CvStages;
+template <> struct CvStages<__nv_bfloat16> { static constexpr int n = 3; };  // 3 x 33.5 KB, two CTAs per SM
+template <> struct CvStages<float> { static constexpr int n = 2; };          // 2 x 67 KB
+
+// 8 channels of one staged row (the lane's 16 bytes of bf16, or 32 bytes of f32)
+__device__ __forceinline__ void row8(const uint8_t *row, int lane, float (&x)[8], const __nv_bfloat16 *) {
+    Vec8<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(row + 16 * lane), x);
+}
+__device__ __forceinline__ void row8(const uint8_t *row, int lane, float (&x)[8], const float *) {
+    const float4 a = *reinterpret_cast<const float4 *>(row + 32 * lane);
+    const float4 b = *reinterpret_cast<const float4 *>(row + 32 * lane + 16);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
-conv_prefill_kernel(const T *__restrict__ x, const float *__restrict__ w, const float *__restrict__ b,
+__global__ void __launch_bounds__(kCvThreads, 2)
+conv_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const float *__restrict__ w, const float *__restrict__ b,
                     const float *__restrict__ st_in, float *__restrict__ st_out, T *__restrict__ y, int64_t rows,
-                    int nseq, int Tlen, int D, const int32_t *__restrict__ cu) {
-    // a warp covers 256 channels (512 contiguous bytes per row) of a run of kRun rows; a thread keeps
-    // the three inputs before its current row in registers and loads its whole run at once
-    const int c0 = (blockIdx.y * 32 + (threadIdx.x & 31)) * kVec;
-    const int64_t r0 = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRun;
-    if (c0 >= D || r0 >= rows) return;
-    const int64_t valid_rows = cu ? (int64_t)__ldg(cu + nseq) : rows;  // rows past the last sequence: untouched
-    if (r0 >= valid_rows) return;
-    const int64_t r1 = (r0 + kRun < valid_rows) ? r0 + kRun : valid_rows;
-    typename Vec8<T>::Raw xr[kRun];
-#pragma unroll
-    for (int j = 0; j < kRun; ++j)
-        if (r0 + j < r1) xr[j] = Vec8<T>::load_raw(x + (size_t)(r0 + j) * D + c0);
-    int64_t start, end;
-    int s = seq_of(r0, nseq, Tlen, cu, start, end);
-    if (start < 0 || start > r0 || end <= r0 || end > rows) {
-        record_status(GLA_ERR_DEVICE_ARG);
-        return;
+                    int nseq, int Tlen, int D, int slab, const int32_t *__restrict__ cu, int64_t ntiles) {
+    using namespace ptx;
+    constexpr int NST = CvStages<T>::n;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t row_bytes = (uint32_t)slab * sizeof(T);
+    const uint32_t stage_bytes = (uint32_t)kCvBoxRows * row_bytes;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + NST * stage_bytes;  // 8-byte aligned: row_bytes is a multiple of 16
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + NST * stage_bytes + 16 * NST);
+    auto full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
+    auto empty = [&](int st) { return bar0 + 8u * (uint32_t)(NST + st); };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cbase = blockIdx.y * slab;
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int st = 0; st < NST; ++st) {
+            mbar_init(full(st), 1);
+            mbar_init(empty(st), kCvWarps);
+        }
+        fence_mbar_init();
     }
-    float h[3][8];  // x_{t-3}, x_{t-2}, x_{t-1}
-    auto fill_history = [&](int64_t row) {
-        for (int m = 0; m < 3; ++m) {
-            const int64_t q = row - 3 + m;  // absolute row of that input
-            if (q >= start) {
-                Vec8<T>::unpack(Vec8<T>::load_raw(x + (size_t)q * D + c0), h[m]);
-            } else {
-                const int idx = (int)(q - start) + 3;  // 0..2 within the incoming state
-#pragma unroll
-                for (int i = 0; i < kVec; ++i)
-                    h[m][i] = st_in ? __ldg(st_in + ((size_t)s * D + c0 + i) * 3 + idx) : 0.f;
+    __syncthreads();
+
+    if (warp == kCvWarps) {
+        // ---- producer: one TMA box per tile, box row k = row t * 64 - 3 + k ----
+        if (lane == 0) {
+            tma_prefetch_desc(&tmX);
+            int64_t i = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int st = (int)(i % NST);
+                if (i >= NST && !mbar_wait(empty(st), (uint32_t)((i / NST) - 1) & 1u, abort_flag, kCvWaitNs)) {
+                    record_status(GLA_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_expect_tx(full(st), stage_bytes);
+                tma_load_2d(sbase + (uint32_t)st * stage_bytes, &tmX, cbase, (int32_t)(t * kCvTile - 3), full(st));
             }
         }
-    };
-    fill_history(r0);
+        return;
+    }
+
+    // ---- compute warps ----
+    const int c0 = cbase + 8 * lane;
+    const bool active = 8 * lane < slab && c0 < D;
+    const int64_t valid_rows = cu ? (int64_t)__ldg(cu + nseq) : rows;  // rows past the last sequence: untouched
+    // for bf16 outputs SiLU is computed as hz + hz tanh(hz) with hz = z / 2, so the fast path carries the
+    // weights and bias halved (exact: a power of two)
+    constexpr float kZs = sizeof(T) == 2 ? 0.5f : 1.f;
     float wt[4][8], bias[8];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
-        const float4 t = __ldg(reinterpret_cast<const float4 *>(w + (size_t)(c0 + i) * 4));
-        wt[0][i] = t.x; wt[1][i] = t.y; wt[2][i] = t.z; wt[3][i] = t.w;
-        bias[i] = b ? __ldg(b + c0 + i) : 0.f;
+        const float4 t4 = active ? __ldg(reinterpret_cast<const float4 *>(w + (size_t)(c0 + i) * 4))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        wt[0][i] = kZs * t4.x; wt[1][i] = kZs * t4.y; wt[2][i] = kZs * t4.z; wt[3][i] = kZs * t4.w;
+        bias[i] = (active && b) ? kZs * __ldg(b + c0 + i) : 0.f;
     }
+    int64_t i = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        const int st = (int)(i % NST);
+        if (!mbar_wait(full(st), (uint32_t)(i / NST) & 1u, abort_flag, kCvWaitNs)) {
+            record_status(GLA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return;
+        }
+        const uint8_t *box = smem + (size_t)st * stage_bytes;  // box row k holds row t * 64 - 3 + k
+        const uint8_t *wbox = box + (size_t)warp * kCvRun * row_bytes;  // this warp's rows start at box row 3
+        const int64_t r0 = t * kCvTile + (int64_t)warp * kCvRun;
+        const int64_t r1 = (r0 + kCvRun < valid_rows) ? r0 + kCvRun : valid_rows;
+        bool bad = false;
+        if (active && r0 < r1) {
+            int64_t start, end;
+            int s = seq_of(r0, nseq, Tlen, cu, start, end);
+            bad = start < 0 || start > r0 || end <= r0 || end > rows;
+            if (!bad && r1 == r0 + kCvRun && start <= r0 - 3 && end >= r0 + kCvRun) {
+                // fast path: the run and its three inputs before lie inside one sequence; fully unrolled,
+                // so the window of the last four rows lives in registers without copies
+                float xw[kCvRun + 3][8];
 #pragma unroll
-    for (int j = 0; j < kRun; ++j) {
-        const int64_t row = r0 + j;
-        if (row >= r1) break;
-        if (row >= end) {  // the next sequence starts inside this run
-            s = seq_of(row, nseq, Tlen, cu, start, end);
-            if (start < 0 || start > row || end <= row || end > rows) {
-                record_status(GLA_ERR_DEVICE_ARG);
-                return;
+                for (int m = 0; m < 3; ++m) row8(wbox + (size_t)m * row_bytes, lane, xw[m], (const T *)nullptr);
+                T *yp = y + (size_t)r0 * D + c0;
+#pragma unroll
+                for (int j = 0; j < kCvRun; ++j) {
+                    row8(wbox + (size_t)(j + 3) * row_bytes, lane, xw[j + 3], (const T *)nullptr);
+                    float out[8];
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) {
+                        const float z = fmaf(wt[3][e], xw[j + 3][e],
+                                             fmaf(wt[2][e], xw[j + 2][e], fmaf(wt[1][e], xw[j + 1][e], fmaf(wt[0][e], xw[j][e], bias[e]))));
+                        out[e] = silu_scaled<T>(z);
+                    }
+                    Vec8<T>::store(yp + (size_t)j * D, out);
+                }
+                if (end == r0 + kCvRun && st_out) {  // the run ends its sequence: the conv state
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e)
+#pragma unroll
+                        for (int m = 0; m < 3; ++m) st_out[((size_t)s * D + c0 + e) * 3 + m] = xw[kCvRun + m][e];
+                }
+            } else if (!bad) {
+                float h[3][8];  // x_{t-3}, x_{t-2}, x_{t-1}
+                // inputs before `row`: staged rows, or the incoming conv state before the sequence start
+                auto fill_history = [&](int64_t row) {
+                    for (int m = 0; m < 3; ++m) {
+                        const int64_t q = row - 3 + m;
+                        if (q >= start) {
+                            row8(box + (size_t)(q - (t * kCvTile - 3)) * row_bytes, lane, h[m], (const T *)nullptr);
+                        } else {
+                            const int idx = (int)(q - start) + 3;  // 0..2 within the incoming state
+#pragma unroll
+                            for (int e = 0; e < kVec; ++e)
+                                h[m][e] = st_in ? __ldg(st_in + ((size_t)s * D + c0 + e) * 3 + idx) : 0.f;
+                        }
+                    }
+                };
+                fill_history(r0);
+                for (int j = 0; j < kCvRun; ++j) {
+                    const int64_t row = r0 + j;
+                    if (row >= r1) break;
+                    if (row >= end) {  // the next sequence starts inside this run
+                        s = seq_of(row, nseq, Tlen, cu, start, end);
+                        if (start < 0 || start > row || end <= row || end > rows) {
+                            bad = true;
+                            break;
+                        }
+                        fill_history(row);
+                    }
+                    float xt[8], out[8];
+                    row8(wbox + (size_t)(3 + j) * row_bytes, lane, xt, (const T *)nullptr);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) {
+                        const float z = fmaf(wt[3][e], xt[e], fmaf(wt[2][e], h[2][e], fmaf(wt[1][e], h[1][e], fmaf(wt[0][e], h[0][e], bias[e]))));
+                        out[e] = silu_scaled<T>(z);
+                        h[0][e] = h[1][e];
+                        h[1][e] = h[2][e];
+                        h[2][e] = xt[e];
+                    }
+                    Vec8<T>::store(y + (size_t)row * D + c0, out);
+                    if (row == end - 1 && st_out) {  // last token of the sequence: its conv state
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e)
+#pragma unroll
+                            for (int m = 0; m < 3; ++m) st_out[((size_t)s * D + c0 + e) * 3 + m] = h[m][e];
+                    }
+                }
             }
-            fill_history(row);
         }
-        float xt[8], out[8];
-        Vec8<T>::unpack(xr[j], xt);
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) {
-            const float z = bias[i] + wt[0][i] * h[0][i] + wt[1][i] * h[1][i] + wt[2][i] * h[2][i] + wt[3][i] * xt[i];
-            out[i] = silu_t<T>(z);
-            h[0][i] = h[1][i];
-            h[1][i] = h[2][i];
-            h[2][i] = xt[i];
-        }
-        Vec8<T>::store(y + (size_t)row * D + c0, out);
-        if (row == end - 1 && st_out) {  // last token of the sequence: its conv state
-#pragma unroll
-            for (int i = 0; i < kVec; ++i)
-#pragma unroll
-                for (int m = 0; m < 3; ++m) st_out[((size_t)s * D + c0 + i) * 3 + m] = h[m][i];
-        }
+        if (bad) record_status(GLA_ERR_DEVICE_ARG);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(st));  // this warp is done with the stage
     }
 }
 
@@ -246,16 +355,59 @@ conv_step_kernel(const T *__restrict__ x, const float *__restrict__ w, const flo
 
 }  // namespace
 
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base, uint64_t cols,
+                 uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw);
+
+// CTAs of the prefill kernel an SM holds at once (looked up once per device and element type)
+template <typename T>
+static int resident_ctas(size_t bytes) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = -1;
+    if (dev >= 0) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv_prefill_kernel<T>, kCvThreads, bytes) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        return 1;
+    }
+    if (dev >= 0) cache[dev].store(per_sm, std::memory_order_relaxed);
+    return per_sm;
+}
+
 template <typename T>
 static int conv_prefill(const T *x, const float *w, const float *b, const float *st_in, float *st_out, T *y, int nseq,
                         int Tlen, int D, const int32_t *cu, cudaStream_t st) {
     const int64_t rows = cu ? (int64_t)Tlen : (int64_t)nseq * Tlen;
-    const int64_t tiles = (rows + kRun * (kThreads / 32) - 1) / (kRun * (kThreads / 32));
-    const int cgroups = (D / kVec + 31) / 32;
-    if (tiles > 0x7fffffffLL || cgroups > 65535) return GLA_ERR_UNSUPPORTED;
+    if (rows >= (1ll << 31) - kCvTile) return GLA_ERR_UNSUPPORTED;
     if (rows > 0) {
-        dim3 grid((unsigned)tiles, (unsigned)cgroups);
-        conv_prefill_kernel<T><<<grid, kThreads, 0, st>>>(x, w, b, st_in, st_out, y, rows, nseq, Tlen, D, cu);
+        const int slab = D < kCvSlab ? D : kCvSlab;  // a multiple of 8 (D % 8 == 0)
+        const int64_t nslabs = (D + slab - 1) / slab;
+        const int64_t ntiles = (rows + kCvTile - 1) / kCvTile;
+        if (nslabs > 65535) return GLA_ERR_UNSUPPORTED;
+        CUtensorMap m;
+        const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        if (!make_map_2d(&m, dt, (uint32_t)sizeof(T), x, (uint64_t)D, (uint64_t)rows, (uint32_t)slab, kCvBoxRows,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GLA_ERR_LAUNCH;
+        constexpr int NST = CvStages<T>::n;
+        const size_t bytes = (size_t)NST * kCvBoxRows * slab * sizeof(T) + 16 * NST + 16;
+        if (cudaFuncSetAttribute(conv_prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+            cudaSuccess)
+            return GLA_ERR_LAUNCH;
+        // one wave: as many CTAs as the SMs hold at once (rounded down to whole slabs), each walking tiles
+        // t, t + gridDim.x, ...; a second partial wave would double the time of its tiles
+        const int per_sm = resident_ctas<T>(bytes);
+        int64_t gx = (int64_t)per_sm * device_info().sm_count / nslabs;
+        gx = gx < 1 ? 1 : gx;
+        gx = gx < ntiles ? gx : ntiles;
+        dim3 grid((unsigned)gx, (unsigned)nslabs);
+        conv_prefill_kernel<T><<<grid, kCvThreads, bytes, st>>>(m, w, b, st_in, st_out, y, rows, nseq, Tlen, D, slab,
+                                                                cu, ntiles);
         count_launches(1);
     }
     if (cu != nullptr && st_out != nullptr && nseq > 0) {

@@ -990,6 +990,19 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D tensor map of any element type over [rows, cols] (row stride cols * elem_bytes), box box_rows x box_cols.
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base, uint64_t cols,
+                 uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * elem_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
               CUtensorMapSwizzle sw) {

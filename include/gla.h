@@ -290,7 +290,7 @@ GLA_API int gla_decode_step_paged(const void *q, const void *k, const void *v, c
  *
  *   x, y         [B, T, D] bf16 (packed [1, T, D] with cu_seqlens, and then B
  *                is the number of sequences N; rows past cu_seqlens[N] are
- *                neither read nor written)
+ *                never written, though tiles that reach into them may read them)
  *   weight       [D, 4] f32;  bias [D] f32 or NULL
  *   state_in     [B|N, D, 3] f32 or NULL (zeros);  state_out [B|N, D, 3] f32 or NULL
  *   D % 8 == 0; every pointer 16-byte aligned.  Memory-bound: x is read and y

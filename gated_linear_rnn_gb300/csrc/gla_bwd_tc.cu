@@ -23,7 +23,8 @@
 //   stronger decays return at once (their gradients come from the chunked SIMT
 //   backward, which the host runs for those heads only).
 //
-// Per CTA (128 threads; thread t owns TMEM lane t):
+// Per CTA (256 threads; warps w and w + 4 share TMEM lane quadrant w, and so row 32 w + lane; the
+// masks split each row's 128 score columns between the two, the epilogue its three accumulators):
 //   TMA:   Q, K tiles [128 x dk] (64B swizzle), V, dO tiles [128 x dv] (128B
 //          swizzle), the two bf16 state tiles as raw images (bulk copies)
 //   MMA1   A^T = K Q^T            -> scratch [384, 512)   mask -> P1 (bf16)
@@ -55,7 +56,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kC = 128;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // two warps per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColScratch = 384;
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;
@@ -112,23 +113,34 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&p)[16
 
 // Mask the 128 x 128 f32 scores in the scratch columns into bf16 P (in place, 64 columns).  Row r
 // of this thread; element (r, x) is kept when (lower ? x <= r : x >= r) and both are below L, and
-// is multiplied by colf[x].
-__device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool lower, const float *colf) {
+// is multiplied by colf[x].  The two warps of a lane quadrant take score columns [64 half, 64 half + 64)
+// each; P block b (16 columns) overwrites score block b / 2, which the other half may still read, so
+// every thread holds its scores in registers before the CTA barrier and writes P after it.  The barrier
+// is reached by every thread (also when `live` is false: then the warp only passes it).
+__device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool lower, const float *colf, int half,
+                                            bool live) {
     const bool row_ok = r < L;
-#pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
-        uint32_t a[32], p[16];
-        tmem_ld32(tbase + (uint32_t)(32 * b), a);
+    uint32_t a[2][32];
+    if (live) {
+        tmem_ld32(tbase + (uint32_t)(64 * half), a[0]);
+        tmem_ld32(tbase + (uint32_t)(64 * half + 32), a[1]);
         tmem_wait_ld();
+    }
+    named_bar_sync(1, kThreads);
+    if (!live) return;
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+        const int b = 2 * half + bb;
+        uint32_t p[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int x0 = 32 * b + 2 * e, x1 = x0 + 1;
             const bool k0 = row_ok && x0 < L && (lower ? x0 <= r : x0 >= r);
             const bool k1 = row_ok && x1 < L && (lower ? x1 <= r : x1 >= r);
-            p[e] = pack_bf16x2(k0 ? __uint_as_float(a[2 * e]) * colf[x0] : 0.f,
-                               k1 ? __uint_as_float(a[2 * e + 1]) * colf[x1] : 0.f);
+            p[e] = pack_bf16x2(k0 ? __uint_as_float(a[bb][2 * e]) * colf[x0] : 0.f,
+                               k1 ? __uint_as_float(a[bb][2 * e + 1]) * colf[x1] : 0.f);
         }
-        tmem_st16(tbase + (uint32_t)(16 * b), p);  // block b's P columns only overwrite scores already read
+        tmem_st16(tbase + (uint32_t)(16 * b), p);
     }
     tmem_wait_st();
 }
@@ -189,6 +201,8 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const int nka = dk / 32, nva = dv / 64;
     const int slot = blockIdx.x / H, h = blockIdx.x % H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant; which half of the work
+    const int r = 32 * quad + lane;              // this thread's row (TMEM lane)
 
     const float ld = __ldg(P.log_decay + h);
     if (!(ld >= kFactoredMinLogDecay)) return;  // strong decay: the SIMT backward owns this head
@@ -233,12 +247,11 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mbar_init(BAR(B_LOAD2), 1);
         mbar_init(BAR(B_LOAD3), 1);
         mbar_init(BAR(B_MMA), 1);
-        mbar_init(BAR(B_MASK), 4);
+        mbar_init(BAR(B_MASK), kThreads / 32);
         mbar_init(BAR(B_FINAL), 1);
         fence_mbar_init();
     }
-    tab[tid] = expf((float)tid * ld);
-    if (tid == 0) tab[kC] = expf((float)kC * ld);
+    if (tid <= kC) tab[tid] = expf((float)tid * ld);
     if (tid < kC) utab[tid] = expf(-(float)(tid + 1) * ld);
     if (warp == 0) {
         tmem_alloc(sb + plan.slot, tcols);
@@ -248,7 +261,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<uint32_t *>(smem + plan.slot);
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const uint32_t colDV = 0, colDK = (uint32_t)dv, colDQ = (uint32_t)(dv + dk);
     const int64_t img = ((int64_t)slot * H + h) * dk * dv;
 
@@ -314,7 +327,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mma_commit(BAR(B_MMA));
     }
     // column factors of the dV / dK masks: lambda^(i+1-L); of the dQ mask: lambda^-(j+1) (utab)
-    wcol[tid] = tab[min(tid + 1, kC)] * utab[max(L - 1, 0)];
+    if (tid < kC) wcol[tid] = tab[min(tid + 1, kC)] * utab[max(L - 1, 0)];
     __syncthreads();
 
     int mma_phase = 0, mask_phase = 0;
@@ -325,7 +338,8 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tc_fence_after();
     };
     auto masked = [&](bool lower, const float *colf) {
-        if (ok) mask_scores(tmem + lane_base + kColScratch, tid, L, lower, colf);
+        // TMEM loads and stores are warp-collective: a warp takes part only if all its lanes are fine
+        mask_scores(tmem + lane_base + kColScratch, r, L, lower, colf, half, __all_sync(0xffffffffu, ok) != 0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(B_MASK));
@@ -389,15 +403,18 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     // ---- epilogue: row factors, bf16, rows below L ----
     ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA: the epilogue has a barrier
     if (ok) {
-        const int r = tid;
         const float rf = tab[max(L - 1 - r, 0)];  // lambda^(L-1-j) for dV and dK
         const float qf = tab[min(r + 1, kC)];     // lambda^(i+1) for dQ
+        // the first half of the warps takes dV (dv columns), the second dK and dQ (2 dk columns)
         if (L == kC) {
             // a full chunk: every tile is free now; stage the rows as TMA boxes (dV over V, dK over K,
             // dQ over Q) and write them with one store per atom
-            stage_row(tmem + lane_base + colDV, dv, rf, r, smem + plan.v, 64);
-            stage_row(tmem + lane_base + colDK, dk, rf, r, smem + plan.k, 32);
-            stage_row(tmem + lane_base + colDQ, dk, qf, r, smem + plan.q, 32);
+            if (half == 0) {
+                stage_row(tmem + lane_base + colDV, dv, rf, r, smem + plan.v, 64);
+            } else {
+                stage_row(tmem + lane_base + colDK, dk, rf, r, smem + plan.k, 32);
+                stage_row(tmem + lane_base + colDQ, dk, qf, r, smem + plan.q, 32);
+            }
             fence_async_shared();
             __syncthreads();
             if (tid == 0) {
@@ -414,9 +431,12 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // the last chunk of a sequence: rows from L on belong to the next one; plain stores
             const bool live = r < L;
             const int64_t row = row0 + (r < L ? r : 0);
-            store_row(tmem + lane_base + colDV, dv, rf, live, P.dv + (row * H + h) * dv);
-            store_row(tmem + lane_base + colDK, dk, rf, live, P.dk + (row * H + h) * dk);
-            store_row(tmem + lane_base + colDQ, dk, qf, live, P.dq + (row * H + h) * dk);
+            if (half == 0) {
+                store_row(tmem + lane_base + colDV, dv, rf, live, P.dv + (row * H + h) * dv);
+            } else {
+                store_row(tmem + lane_base + colDK, dk, rf, live, P.dk + (row * H + h) * dk);
+                store_row(tmem + lane_base + colDQ, dk, qf, live, P.dq + (row * H + h) * dk);
+            }
         }
     } else if (tid == 0) {
         record_status(GLA_ERR_TIMEOUT);

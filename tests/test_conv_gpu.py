@@ -95,3 +95,26 @@ def test_conv_layer_shape():
     y_ref, so_ref = oracle.conv1d_silu(x, w, b)
     assert oracle.rel_err(y.float().cpu().numpy(), y_ref) <= 1e-2
     assert np.array_equal(so.cpu().numpy(), so_ref)
+
+
+@pytest.mark.parametrize("D", [264, 520, 2056])
+def test_conv_partial_channel_slab(D):
+    """Channel counts that leave a partial last 256-channel slab (the TMA box reaches past D)."""
+    x, w, b, st = make((2, 150), D, torch.bfloat16, seed=D, nseq=2)
+    y, so = run_conv(x, w, b, st)
+    y_ref, so_ref = oracle.conv1d_silu(x, w, b, st)
+    assert oracle.rel_err(y.float().cpu().numpy(), y_ref) <= 1e-2
+    assert np.array_equal(so.cpu().numpy(), so_ref)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_conv_ragged_across_tiles(dtype):
+    """Sequences that start and end on either side of 64-row tile and 8-row run boundaries."""
+    lens = [64, 1, 63, 130, 3, 8, 0, 200, 7, 61, 2]
+    total = sum(lens)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    x, w, b, st = make((1, total), 512, dtype, seed=7, nseq=len(lens))
+    y, so = run_conv(x, w, b, st, cu)
+    y_ref, so_ref = oracle.conv1d_silu(x, w, b, st, cu_seqlens=cu.numpy())
+    assert oracle.rel_err(y.float().cpu().numpy(), y_ref) <= TOL[dtype]
+    assert np.array_equal(so.cpu().numpy(), so_ref)

@@ -28,7 +28,6 @@ GLA_DEFINE_STATUS(conv)
 namespace gla {
 namespace {
 
-constexpr int kThreads = 256;  // step kernel: 2048 channels per block
 constexpr int kVec = 8;        // channels per thread
 
 template <typename T>
@@ -322,35 +321,61 @@ __global__ void conv_empty_kernel(const float *__restrict__ st_in, float *__rest
         st_out[(size_t)s * D * 3 + e] = st_in ? st_in[(size_t)s * D * 3 + e] : 0.f;
 }
 
+// Step: a block owns 1024 channels (8 per thread) of kStepSeqs sequences, so the weights and bias
+// are read once per block and reused; two sequences' x and state are in flight at a time.
+constexpr int kStepThreads = 128;
+constexpr int kStepSeqs = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kStepThreads)
 conv_step_kernel(const T *__restrict__ x, const float *__restrict__ w, const float *__restrict__ b,
                  float *__restrict__ state, T *__restrict__ y, int N, int D) {
-    const int c0 = (blockIdx.x * kThreads + threadIdx.x) * kVec;
-    const int n = blockIdx.y;
-    if (c0 >= D || n >= N) return;
-    float xt[8], out[8];
-    Vec8<T>::load(x + (size_t)n * D + c0, xt);
-    float4 *sp = reinterpret_cast<float4 *>(state + ((size_t)n * D + c0) * 3);  // 24 floats, 16-byte aligned
-    float hs[24];
-#pragma unroll
-    for (int j = 0; j < 6; ++j) {
-        const float4 t = sp[j];
-        hs[4 * j] = t.x; hs[4 * j + 1] = t.y; hs[4 * j + 2] = t.z; hs[4 * j + 3] = t.w;
-    }
+    const int c0 = (blockIdx.x * kStepThreads + threadIdx.x) * kVec;
+    if (c0 >= D) return;
+    const int n0 = blockIdx.y * kStepSeqs;
+    float wt[4][8], bias[8];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
         const float4 t = __ldg(reinterpret_cast<const float4 *>(w + (size_t)(c0 + i) * 4));
-        const float z = (b ? __ldg(b + c0 + i) : 0.f) + t.x * hs[3 * i] + t.y * hs[3 * i + 1] + t.z * hs[3 * i + 2] +
-                        t.w * xt[i];
-        out[i] = silu(z);
-        hs[3 * i] = hs[3 * i + 1];
-        hs[3 * i + 1] = hs[3 * i + 2];
-        hs[3 * i + 2] = xt[i];
+        wt[0][i] = t.x; wt[1][i] = t.y; wt[2][i] = t.z; wt[3][i] = t.w;
+        bias[i] = b ? __ldg(b + c0 + i) : 0.f;
     }
+#pragma unroll 1
+    for (int nn = 0; nn < kStepSeqs; nn += 2) {
+        float xt[2][8], hs[2][24];
 #pragma unroll
-    for (int j = 0; j < 6; ++j) sp[j] = make_float4(hs[4 * j], hs[4 * j + 1], hs[4 * j + 2], hs[4 * j + 3]);
-    Vec8<T>::store(y + (size_t)n * D + c0, out);
+        for (int u = 0; u < 2; ++u) {
+            const int n = n0 + nn + u;
+            if (n >= N) continue;
+            Vec8<T>::load(x + (size_t)n * D + c0, xt[u]);
+            const float4 *sp = reinterpret_cast<const float4 *>(state + ((size_t)n * D + c0) * 3);  // 24 floats
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                const float4 t = sp[j];
+                hs[u][4 * j] = t.x; hs[u][4 * j + 1] = t.y; hs[u][4 * j + 2] = t.z; hs[u][4 * j + 3] = t.w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int n = n0 + nn + u;
+            if (n >= N) continue;
+            float out[8];
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) {
+                const float z = bias[i] + wt[0][i] * hs[u][3 * i] + wt[1][i] * hs[u][3 * i + 1] +
+                                wt[2][i] * hs[u][3 * i + 2] + wt[3][i] * xt[u][i];
+                out[i] = silu(z);
+                hs[u][3 * i] = hs[u][3 * i + 1];
+                hs[u][3 * i + 1] = hs[u][3 * i + 2];
+                hs[u][3 * i + 2] = xt[u][i];
+            }
+            float4 *sp = reinterpret_cast<float4 *>(state + ((size_t)n * D + c0) * 3);
+#pragma unroll
+            for (int j = 0; j < 6; ++j)
+                sp[j] = make_float4(hs[u][4 * j], hs[u][4 * j + 1], hs[u][4 * j + 2], hs[u][4 * j + 3]);
+            Vec8<T>::store(y + (size_t)n * D + c0, out);
+        }
+    }
 }
 
 }  // namespace
@@ -431,10 +456,12 @@ int conv1d_silu_f32(const float *x, const float *w, const float *b, const float 
 int conv1d_silu_step_bf16(const void *x, const float *w, const float *b, float *state, void *y, int N, int D,
                           cudaStream_t st) {
     using B = __nv_bfloat16;
-    const int cgroups = (D / kVec + kThreads - 1) / kThreads;
-    if (N > 65535) return GLA_ERR_UNSUPPORTED;
-    dim3 grid((unsigned)cgroups, (unsigned)N);
-    conv_step_kernel<B><<<grid, kThreads, 0, st>>>((const B *)x, w, b, state, (B *)y, N, D);
+    const int cgroups = (D / kVec + kStepThreads - 1) / kStepThreads;
+    const int ngroups = (N + kStepSeqs - 1) / kStepSeqs;
+    if (N <= 0) return GLA_OK;
+    if (ngroups > 65535) return GLA_ERR_UNSUPPORTED;
+    dim3 grid((unsigned)cgroups, (unsigned)ngroups);
+    conv_step_kernel<B><<<grid, kStepThreads, 0, st>>>((const B *)x, w, b, state, (B *)y, N, D);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }

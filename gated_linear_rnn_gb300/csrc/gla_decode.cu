@@ -62,10 +62,17 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const int ncg = dv >> 2;
     const int tid = threadIdx.x;
     const int cg = tid % ncg, rg = tid / ncg;
+    // the slot (paged form) and q, k, v are independent loads: all in flight at once
+    const int slot = slots != nullptr ? __ldg(slots + unit / H) : 0;
+    for (int i = tid; i < dk; i += blockDim.x) {
+        qs[i] = to_f32(q[(size_t)unit * dk + i]);
+        ks[i] = to_f32(k[(size_t)unit * dk + i]);
+    }
+    float vv[4];
+    load4<T>(v + (size_t)unit * dv + cg * 4, vv);
+    const float lam = expf(__ldg(log_decay + h));
     size_t page = (size_t)unit;  // state page of this (n, h): unit itself unless paged
     if (slots != nullptr) {
-        const int n = unit / H;
-        const int slot = __ldg(slots + n);
         if (slot < 0 || slot >= nslots) {  // padding row (or a bad slot, reported): zero output, no page
             if (slot >= nslots && tid == 0) record_status(GLA_ERR_DEVICE_ARG);
             for (int c = tid; c < dv; c += blockDim.x) out[(size_t)unit * dv + c] = from_f32<T>(0.f);
@@ -74,24 +81,24 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         page = (size_t)slot * H + h;
     }
 
-    for (int i = tid; i < dk; i += blockDim.x) {
-        qs[i] = to_f32(q[(size_t)unit * dk + i]);
-        ks[i] = to_f32(k[(size_t)unit * dk + i]);
-    }
-    float vv[4];
-    load4<T>(v + (size_t)unit * dv + cg * 4, vv);
-    const float lam = expf(__ldg(log_decay + h));
-    __syncthreads();
-
     float4 *S = reinterpret_cast<float4 *>(state + page * dk * dv) + cg;
     const int row_f4 = ncg;  // float4 per state row
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r0 = rg; r0 < dk; r0 += kRG * kUnroll) {
-        float4 s[kUnroll];
+    float4 s[kUnroll];
+    // the first rows of state need neither q nor k: in flight before the block barrier
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int r = r0 + u * kRG;
-            if (r < dk) s[u] = __ldcs(S + (size_t)r * row_f4);
+    for (int u = 0; u < kUnroll; ++u) {
+        const int r = rg + u * kRG;
+        if (r < dk) s[u] = __ldcs(S + (size_t)r * row_f4);
+    }
+    __syncthreads();
+    for (int r0 = rg; r0 < dk; r0 += kRG * kUnroll) {
+        if (r0 != rg) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int r = r0 + u * kRG;
+                if (r < dk) s[u] = __ldcs(S + (size_t)r * row_f4);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {

@@ -208,6 +208,35 @@ def test_single_token_prefill_equals_decode_step():
     assert oracle.rel_err(h_pre.cpu().numpy(), s.cpu().numpy()) <= 1e-2
 
 
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_steps_follow_the_prefill_token_by_token(dtype):
+    """Serving continuity: T recurrent decode steps from h0 reproduce the chunked prefill over the same
+    T tokens, output by output and in the final state (T = 200 crosses a chunk boundary and ends in a
+    partial chunk; the bf16 prefill runs on the tensor-core kernel).  Both sides are also held to the
+    fp64 recurrence."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"] if dtype == "bf16" else I.WORKLOADS["tiny_f32"], B=2, T=200, H=4,
+                 dk=96, dv=192, h0_std=0.02, dtype=dtype)
+    d = I.make_prefill(w, device="cuda", seed=31)
+    o_pre, h_pre = gla.chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], chunk=128 if dtype == "bf16" else 64)
+    state = d["h0"].clone()
+    o_dec = torch.empty_like(o_pre)
+    for t in range(w.T):
+        o_dec[:, t] = gla.decode_step(d["q"][:, t].contiguous(), d["k"][:, t].contiguous(), d["v"][:, t].contiguous(),
+                                      d["log_decay"], state)
+    torch.cuda.synchronize()
+    assert gla.gla_last_device_status() == 0
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    tol = TOL[dtype]
+    pre, dec = o_pre.float().cpu().numpy(), o_dec.float().cpu().numpy()
+    assert oracle.rel_err(pre, o_ref) <= tol and oracle.rel_err(dec, o_ref) <= tol
+    assert oracle.rel_err(dec, pre) <= 2 * tol
+    for t in (0, 127, 128, 199):  # token by token at the chunk edges as well
+        assert oracle.rel_err(dec[:, t], pre[:, t]) <= 2 * tol, t
+    assert oracle.rel_err(state.cpu().numpy(), h_ref) <= tol
+    assert oracle.rel_err(state.cpu().numpy(), h_pre.cpu().numpy()) <= 2 * tol
+
+
 # ---- decode ----
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("dk,dv", [(96, 192), (64, 64), (100, 36), (8, 1024)])

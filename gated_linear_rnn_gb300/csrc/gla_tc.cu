@@ -100,7 +100,13 @@ struct Params {
     int reverse;           // kStates: walk the chunks backwards in time (launches the kRev kernel)
     __nv_bfloat16 *chunk_states;  // kStates: [slots, H, dk*dv] state images; chunk c of sequence s at
                                   // slot start_s / 128 + s + c (start_s its first row)
+    int nseq;              // sequences (packed batches: entries of cu minus one)
+    int lpt;               // packed batch, whole chains: CTA i takes the sequence of length rank i / H
 };
+
+// Packed batches of up to this many sequences are walked longest first (the ranking costs every CTA
+// O(nseq^2 / threads) comparisons in its prologue).
+constexpr int kLptMaxSeq = 256;
 
 // Shared memory plan (bytes from the 1024-aligned base).
 struct Smem {
@@ -201,7 +207,30 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // sequence's last segment to its first
     const int chain = blockIdx.x / P.grid_seg, w = blockIdx.x % P.grid_seg;
     const int seg = rev ? P.nseg - 1 - w : w;  // natural segment
-    const int seq = chain / H, h = chain % H;
+    const int h = chain % H;
+    int seq = chain / H;
+    if (P.lpt) {
+        // Longest sequences first: the CTAs of a packed batch start in blockIdx order as SMs free up, so a
+        // long sequence late in the batch would trail the whole launch.  CTA i takes the sequence whose
+        // length ranks i / H in decreasing order (ties by index: a permutation even for bad offsets, which
+        // seq_range reports below).  The lengths sit in the output staging tiles, unused until the first
+        // epilogue; the pick in the entry after them.
+        int *lens = reinterpret_cast<int *>(smem + plan.xp);
+        for (int s = threadIdx.x; s < P.nseq; s += blockDim.x) lens[s] = __ldg(P.cu + s + 1) - __ldg(P.cu + s);
+        __syncthreads();
+        const int want = chain / H;
+        for (int s = threadIdx.x; s < P.nseq; s += blockDim.x) {
+            const int ls = lens[s];
+            int rank = 0;
+            for (int u = 0; u < P.nseq; ++u) {
+                const int lu = lens[u];
+                rank += (lu > ls || (lu == ls && u < s)) ? 1 : 0;
+            }
+            if (rank == want) lens[P.nseq] = s;
+        }
+        __syncthreads();
+        seq = lens[P.nseq];
+    }
     const bool state_only = P.mode == kStateOnly || P.mode == kStates;
     const bool write_images = P.mode == kStates && P.chunk_states != nullptr;
     const bool segmented = P.mode == kStateOnly || P.mode == kSegmented || (P.mode == kStates && P.nseg > 1);
@@ -1104,9 +1133,11 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.grid_seg = 1;
     p.seg_h0 = nullptr;
     p.seg_end = nullptr;
+    p.nseq = nseq;
     const long long chains = (long long)nseq * H;
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
+    p.lpt = (cu != nullptr && nseg == 1 && nseq > 1 && nseq <= kLptMaxSeq) ? 1 : 0;
     if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, bytes, st);
 
     // segmented schedule: stream-ordered scratch for the segment end / start states
@@ -1174,9 +1205,11 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     p.grid_seg = 1;
     p.reverse = reverse ? 1 : 0;
     p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
+    p.nseq = nseq;
     const long long chains = (long long)nseq * H;
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
+    p.lpt = (cu != nullptr && nseg == 1 && nseq > 1 && nseq <= kLptMaxSeq) ? 1 : 0;
     // the q and out maps are not read in a state-only pass
     if (nseg == 1) return launch_tc(mk, mk, mv, mv, p, chains, bytes, st);
 

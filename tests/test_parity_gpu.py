@@ -103,6 +103,21 @@ def test_ragged_small_with_empty_and_unit_sequences():
     check_prefill(w, lengths=lengths, seed=5)
 
 
+def test_ragged_equal_lengths_take_distinct_sequences():
+    """Packed batches are walked longest first; equal lengths are ranked by index, so every sequence is
+    still taken by exactly one group of CTAs (ties, empty sequences and one long outlier)."""
+    w = I.scaled(I.WORKLOADS["ragged"], H=2)
+    lengths = [5, 5, 0, 200, 5, 200, 0, 5, 1, 1, 700, 5]
+    check_prefill(w, lengths=lengths, seed=12)
+
+
+def test_ragged_many_sequences_launch_order():
+    """More packed sequences than the longest-first ranking takes on: the launch keeps blockIdx order."""
+    w = I.scaled(I.WORKLOADS["ragged"], H=2, dk=32, dv=64)
+    lengths = [(7 * i) % 41 for i in range(300)]
+    check_prefill(w, lengths=lengths, seed=13)
+
+
 def test_decay_extremes():
     """lambda = 1 (log_decay 0) and a vanishing decay in the same launch."""
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=300, H=2, h0_std=0.0)

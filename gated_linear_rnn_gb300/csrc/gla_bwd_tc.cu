@@ -241,6 +241,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + plan.abort);
     const uint32_t tcols = kTmemCols;
 
+    const int64_t img = ((int64_t)slot * H + h) * dk * dv;
     if (tid == 0) {
         *abort_flag = 0;
         mbar_init(BAR(B_LOAD), 1);
@@ -250,30 +251,12 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mbar_init(BAR(B_MASK), kThreads / 32);
         mbar_init(BAR(B_FINAL), 1);
         fence_mbar_init();
-    }
-    if (tid <= kC) tab[tid] = expf((float)tid * ld);
-    if (tid < kC) utab[tid] = expf(-(float)(tid + 1) * ld);
-    if (warp == 0) {
-        tmem_alloc(sb + plan.slot, tcols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<uint32_t *>(smem + plan.slot);
-    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-    const uint32_t colDV = 0, colDK = (uint32_t)dv, colDQ = (uint32_t)(dv + dk);
-    const int64_t img = ((int64_t)slot * H + h) * dk * dv;
-
-    // ---- loads (thread 0) ----
-    if (tid == 0) {
+        // ---- loads, issued before the tables and the TMEM allocation so that those overlap the load
+        // latency (a CTA handles one chunk: its prologue is not amortised) ----
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmDO);
-        tma_prefetch_desc(&tmDQ);
-        tma_prefetch_desc(&tmDK);
-        tma_prefetch_desc(&tmDV);
         const uint32_t st_bytes = (uint32_t)dk * dv * 2u;
         const int y = (int)row0;
         mbar_expect_tx(BAR(B_LOAD), 2u * nka * 8192u);
@@ -289,7 +272,22 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         bulk_load_g2s(sb + plan.g, P.g_img + img, st_bytes, BAR(B_LOAD2));
         mbar_expect_tx(BAR(B_LOAD3), st_bytes);
         bulk_load_g2s(sb + plan.s, P.s_img + img, st_bytes, BAR(B_LOAD3));
+        tma_prefetch_desc(&tmDQ);
+        tma_prefetch_desc(&tmDK);
+        tma_prefetch_desc(&tmDV);
     }
+    if (tid <= kC) tab[tid] = expf((float)tid * ld);
+    if (tid < kC) utab[tid] = expf(-(float)(tid + 1) * ld);
+    if (warp == 0) {
+        tmem_alloc(sb + plan.slot, tcols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<uint32_t *>(smem + plan.slot);
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const uint32_t colDV = 0, colDK = (uint32_t)dv, colDQ = (uint32_t)(dv + dk);
 
     // descriptors
     const uint32_t qb = sb + plan.q, kb = sb + plan.k, vb = sb + plan.v, ob = sb + plan.dout;

@@ -118,3 +118,33 @@ def test_conv_ragged_across_tiles(dtype):
     y_ref, so_ref = oracle.conv1d_silu(x, w, b, st, cu_seqlens=cu.numpy())
     assert oracle.rel_err(y.float().cpu().numpy(), y_ref) <= TOL[dtype]
     assert np.array_equal(so.cpu().numpy(), so_ref)
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_conv_seeded_sweep(case):
+    """Seeded random shapes: D any multiple of 8 (partial 256-channel slabs), dense or packed with
+    empty sequences and rows past the packed total, bf16 or f32, with or without bias and state."""
+    rng = np.random.default_rng(5000 + case)
+    D = 8 * int(rng.integers(1, 520))
+    dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+    cu = None
+    if rng.random() < 0.5:
+        lens = [int(x) for x in rng.integers(0, 200, int(rng.integers(1, 12)))]
+        lens[0] = max(lens[0], 1)
+        total = sum(lens)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+        shape, nseq = (1, total + int(rng.integers(0, 9))), len(lens)
+    else:
+        shape = (int(rng.integers(1, 4)), int(rng.integers(1, 300)))
+        nseq, total = shape[0], shape[1]
+    x, w, b, st = make(shape, D, dtype, seed=case, nseq=nseq, bias=rng.random() < 0.7, state=rng.random() < 0.6)
+    y, so = run_conv(x, w, b, st, cu)
+    yc = y.float().cpu().numpy()
+    if cu is None:
+        y_ref, so_ref = oracle.conv1d_silu(x, w, b, st)
+    else:
+        y_ref, so_ref = oracle.conv1d_silu(x[:, :total], w, b, st, cu_seqlens=cu.numpy())
+        assert np.isnan(yc[:, total:]).all()  # rows past cu_seqlens[N] are not written
+        yc = yc[:, :total]
+    assert oracle.rel_err(yc, y_ref) <= TOL[dtype]
+    assert np.array_equal(so.cpu().numpy(), so_ref)

@@ -353,6 +353,7 @@ def run_ours(args, world, rank, local):
 
     # ---- backward of the layer prefill (training path), timed on its own after the step ----
     bwd = run_backward(args, P, w, stream, peaks, peak_src) if args.bwd_steps > 0 else None
+    train = run_train_step(args, P, w, stream) if args.bwd_steps > 0 else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -378,6 +379,7 @@ def run_ours(args, world, rank, local):
         "decode_paged": paged,
         "conv1d_silu": conv,
         "backward": bwd,
+        "train_step": train,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "wall_s_timed": t_wall,
@@ -503,6 +505,50 @@ def run_backward(args, P, w, stream, peaks, peak_src):
                          "tensor": {"achieved_tflops": tfl, "peak_tflops": peaks["bf16_tflops"],
                                     "frac": tfl / peaks["bf16_tflops"], "flops_per_launch": fl}},
             "kernel": "gla_chunk_bwd (layer_bf16): two tensor-core state passes + chunk-parallel gradient kernel"}
+
+
+def run_train_step(args, P, w, stream):
+    """One training step of the layer (forward, then backward from dout ~ N(0, 1)) two ways: the plain
+    pair gla_chunk_fwd + gla_chunk_bwd, and gla_chunk_fwd_save + gla_chunk_bwd_saved, where the backward
+    takes the states the forward left instead of walking the chains again.  CUDA events per step."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    g = torch.Generator(device=P["q"].device).manual_seed(1000003)
+    do = torch.randn(P["v"].shape, generator=g, device=P["q"].device).to(torch.bfloat16)
+    out = torch.empty_like(do)
+    hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=P["q"].device)
+    dq, dk_, dv_ = (torch.empty_like(P[k]) for k in ("q", "k", "v"))
+    dh0 = torch.empty_like(hT)
+    img = gla.state_images(P["q"], P["v"])
+    q, k, v, ld = P["q"], P["k"], P["v"], P["log_decay"]
+
+    def plain():
+        gla.gla_chunk_fwd(q, k, v, ld, None, out, hT, w.chunk, None, stream)
+        gla.gla_chunk_bwd(q, k, v, do, ld, None, None, dq, dk_, dv_, dh0, w.chunk, None, stream)
+
+    def saved():
+        gla.gla_chunk_fwd_save(q, k, v, ld, None, out, hT, img, w.chunk, None, stream)
+        gla.gla_chunk_bwd_saved(q, k, v, do, ld, None, None, img, dq, dk_, dv_, dh0, w.chunk, None, stream)
+
+    res = {}
+    for name, fn in (("plain_ms", plain), ("saved_states_ms", saved)):
+        for _ in range(3):
+            fn()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.bwd_steps)]
+        for e in ev:
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the training step: {st_code} ({gla.gla_status_str(st_code)})")
+    res.update({"value": w.B * w.T / (res["saved_states_ms"] / 1e3), "unit": "tokens/s",
+                "state_image_bytes": img.numel() * 2, "steps": args.bwd_steps,
+                "note": "forward + backward of the layer; saved_states: the forward writes the state before every "
+                        "chunk and the backward skips its forward state pass"})
+    return res
 
 
 def run_e2e(args, P, D, w, wd, out, hT, dout, stream):

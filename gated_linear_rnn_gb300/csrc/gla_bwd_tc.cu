@@ -467,9 +467,11 @@ bool tc_bwd_supported(int dk, int dv, int chunk) {
 // Backward on the tensor cores: two state passes, the chunk-parallel gradient kernel, then the
 // chunked SIMT backward for the heads whose decay is too strong for the factored masks (its CTAs
 // return at once for every other head).  Scratch: two bf16 state tiles per chunk slot.
-int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *dout, const float *ld,
-                      const float *h0, const float *dhT, void *dq, void *dk_, void *dv_, float *dh0, int nseq,
-                      int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
+// With `s_images` non-null (the states before every chunk, left by the forward) the forward state pass
+// is skipped and only the gradient-state images are scratch.
+static int chunk_bwd_impl(const void *q, const void *k, const void *v, const void *dout, const float *ld, const float *h0,
+                   const float *dhT, const void *s_images, void *dq, void *dk_, void *dv_, float *dh0, int nseq,
+                   int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
     if (!tc_bwd_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
@@ -485,13 +487,16 @@ int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *d
         !make_map(&mdv, dv_, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, kC))
         return GLA_ERR_LAUNCH;
     const size_t per = (size_t)slots * H * dk * dv;  // bf16 elements per image array
+    const size_t nimg = s_images ? 1 : 2;
     __nv_bfloat16 *img = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void **>(&img), 2 * per * sizeof(__nv_bfloat16), st) != cudaSuccess) {
+    if (cudaMallocAsync(reinterpret_cast<void **>(&img), nimg * per * sizeof(__nv_bfloat16), st) != cudaSuccess) {
         cudaGetLastError();
         return GLA_ERR_NOMEM;
     }
-    int rc = tc_state_pass_bf16(k, v, ld, h0, nullptr, img, 0, nseq, Tlen, H, dk, dv, cu, st);
-    if (rc == GLA_OK) rc = tc_state_pass_bf16(q, dout, ld, dhT, dh0, img + per, 1, nseq, Tlen, H, dk, dv, cu, st);
+    const __nv_bfloat16 *s_img = s_images ? reinterpret_cast<const __nv_bfloat16 *>(s_images) : img;
+    __nv_bfloat16 *g_img = img + (nimg - 1) * per;
+    int rc = s_images ? GLA_OK : tc_state_pass_bf16(k, v, ld, h0, nullptr, img, 0, nseq, Tlen, H, dk, dv, cu, st);
+    if (rc == GLA_OK) rc = tc_state_pass_bf16(q, dout, ld, dhT, dh0, g_img, 1, nseq, Tlen, H, dk, dv, cu, st);
     if (rc == GLA_OK) {
         const size_t bytes = bwd_plan(dk, dv).total + 1024;
         if (cudaFuncSetAttribute(gla_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
@@ -501,8 +506,8 @@ int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *d
             BwdParams p{};
             p.log_decay = ld;
             p.cu = cu;
-            p.s_img = img;
-            p.g_img = img + per;
+            p.s_img = s_img;
+            p.g_img = g_img;
             p.dq = reinterpret_cast<__nv_bfloat16 *>(dq);
             p.dk = reinterpret_cast<__nv_bfloat16 *>(dk_);
             p.dv = reinterpret_cast<__nv_bfloat16 *>(dv_);
@@ -522,6 +527,18 @@ int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *d
                                         st);
     cudaFreeAsync(img, st);
     return rc;
+}
+
+int tc_chunk_bwd_bf16(const void *q, const void *k, const void *v, const void *dout, const float *ld,
+                      const float *h0, const float *dhT, void *dq, void *dk_, void *dv_, float *dh0, int nseq,
+                      int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
+    return chunk_bwd_impl(q, k, v, dout, ld, h0, dhT, nullptr, dq, dk_, dv_, dh0, nseq, Tlen, H, dk, dv, cu, st);
+}
+
+int tc_chunk_bwd_bf16_saved(const void *q, const void *k, const void *v, const void *dout, const float *ld,
+                            const float *h0, const float *dhT, const void *s_images, void *dq, void *dk_, void *dv_,
+                            float *dh0, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
+    return chunk_bwd_impl(q, k, v, dout, ld, h0, dhT, s_images, dq, dk_, dv_, dh0, nseq, Tlen, H, dk, dv, cu, st);
 }
 
 }  // namespace gla

@@ -36,6 +36,11 @@ bool tc_bwd_supported(int dk, int dv, int chunk);
 int tc_chunk_bwd_bf16(const void *, const void *, const void *, const void *, const float *, const float *,
                       const float *, void *, void *, void *, float *, int, int, int, int, int, const int32_t *,
                       cudaStream_t);
+int tc_chunk_fwd_bf16_save(const void *, const void *, const void *, const float *, const float *, void *, float *,
+                           void *, int, int, int, int, int, const int32_t *, cudaStream_t);
+int tc_chunk_bwd_bf16_saved(const void *, const void *, const void *, const void *, const float *, const float *,
+                            const float *, const void *, void *, void *, void *, float *, int, int, int, int, int,
+                            const int32_t *, cudaStream_t);
 int conv1d_silu_bf16(const void *, const float *, const float *, const float *, float *, void *, int, int, int,
                      const int32_t *, cudaStream_t);
 int conv1d_silu_f32(const float *, const float *, const float *, const float *, float *, float *, int, int, int,
@@ -194,6 +199,37 @@ int gla_chunk_bwd(const void *q, const void *k, const void *v, const void *dout,
                                  cu_seqlens, (cudaStream_t)stream);
     return simt_chunk_bwd_bf16(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, chunk,
                                cu_seqlens, (cudaStream_t)stream);
+}
+
+long long gla_state_images_bytes(int B, int T, int H, int dk, int dv, int packed) {
+    if (B <= 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 0;
+    const long long rows = packed ? (long long)T : (long long)B * T;
+    return (rows / 128 + B + 1) * (long long)H * dk * dv * 2;
+}
+
+int gla_chunk_fwd_save(const void *q, const void *k, const void *v, const float *log_decay, const float *h0,
+                       void *out, float *hT, void *state_images, int B, int T, int H, int dk, int dv, int chunk,
+                       const int32_t *cu_seqlens, void *stream) {
+    int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    if (!state_images) return GLA_ERR_ARG;
+    if (!aligned16(state_images)) return GLA_ERR_ALIGN;
+    if (!(chunk == 128 && tc_bwd_supported(dk, dv, chunk))) return GLA_ERR_UNSUPPORTED;
+    return tc_chunk_fwd_bf16_save(q, k, v, log_decay, h0, out, hT, state_images, B, T, H, dk, dv, cu_seqlens,
+                                  (cudaStream_t)stream);
+}
+
+int gla_chunk_bwd_saved(const void *q, const void *k, const void *v, const void *dout, const float *log_decay,
+                        const float *h0, const float *dhT, const void *state_images, void *dq, void *dk_out,
+                        void *dv_out, float *dh0, int B, int T, int H, int dk, int dv, int chunk,
+                        const int32_t *cu_seqlens, void *stream) {
+    int rc = check_backward(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    if (!state_images) return GLA_ERR_ARG;
+    if (!aligned16(state_images)) return GLA_ERR_ALIGN;
+    if (!(chunk == 128 && tc_bwd_supported(dk, dv, chunk))) return GLA_ERR_UNSUPPORTED;
+    return tc_chunk_bwd_bf16_saved(q, k, v, dout, log_decay, h0, dhT, state_images, dq, dk_out, dv_out, dh0, B, T, H,
+                                   dk, dv, cu_seqlens, (cudaStream_t)stream);
 }
 
 int gla_chunk_bwd_f32(const float *q, const float *k, const float *v, const float *dout, const float *log_decay,

@@ -233,6 +233,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     }
     const bool state_only = P.mode == kStateOnly || P.mode == kStates;
     const bool write_images = P.mode == kStates && P.chunk_states != nullptr;
+    // The full forward can also leave the state in force before every chunk, as the bf16 tile MMA3 reads,
+    // in the layout the backward consumes (training: the backward then skips its forward state pass).
+    const bool save_images = (P.mode == kWhole || P.mode == kSegmented) && P.chunk_states != nullptr;
     const bool segmented = P.mode == kStateOnly || P.mode == kSegmented || (P.mode == kStates && P.nseg > 1);
 
     SeqRange rng;
@@ -382,7 +385,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // image slot of the state before this segment's first chunk (sequence slot start / 128 + seq,
             // plus the segment's first chunk)
             __nv_bfloat16 *img0 = nullptr;
-            if (write_images) {
+            if (write_images || save_images) {
                 const int ws = blockIdx.x % P.grid_seg;
                 const int64_t first_chunk = P.nseg > 1 ? (int64_t)(rev ? P.nseg - 1 - ws : ws) * P.seg_chunks : 0;
                 img0 = P.chunk_states + ((rng.start / kC + seq + first_chunk) * H + h) * sz_state;
@@ -467,6 +470,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                      (c == 0 || mbar_wait(BAR(B_OFREE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
+                if (save_images) {  // the state copy S_{c-1} just written: out to its image slot
+                    bulk_store_s2g(img0 + (int64_t)c * H * sz_state, sbase + o_s, (uint32_t)(sz_state * 2));
+                    bulk_commit();
+                }
                 // MMA3: O = Q S_{c-1} (factored) or Q' S_{c-1} (direct); A K-major 64B swizzle,
                 // B = S copy, MN-major 128B swizzle
                 for (int kk = 0; kk < ksteps_dk; ++kk) {
@@ -497,7 +504,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 mma_commit(BAR(B_OFULL));
                 mma_commit(BAR(B_KVEMPTY0 + s));  // MMA2 and MMA4 were the last readers of this K/V stage
+                if (save_images) {  // the copy may be refilled once the image store has read it
+                    bulk_wait_read0();
+                    mbar_arrive(BAR(B_IMGDONE));
+                }
             }
+            if (save_images || write_images) bulk_wait_read0();  // no image store may still read shared memory
             if (!ok) {
                 record_status(GLA_ERR_TIMEOUT);
                 *abort_flag = 1;
@@ -707,7 +719,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (early_k && nchunks > 0) ok = prep_k_early(0);
         for (int c = 0; c <= nchunks && ok; ++c) {
             if (c >= 1) {
-                ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
+                ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs) &&
+                     (!save_images || mbar_wait(BAR(B_IMGDONE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -1101,8 +1114,11 @@ int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &m
 
 }  // namespace
 
-int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
-                      float *hT, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
+// The forward on the tensor cores; with `images` non-null the full passes also leave the bf16 state in
+// force before every chunk there ([slots, H, dk, dv], chunk c of sequence s at slot start_s / 128 + s + c).
+static int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
+                   float *hT, void *images, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu,
+                   cudaStream_t st) {
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
@@ -1134,6 +1150,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.seg_h0 = nullptr;
     p.seg_end = nullptr;
     p.nseq = nseq;
+    p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
     const long long chains = (long long)nseq * H;
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
@@ -1153,6 +1170,7 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     p.seg_h0 = scratch + per;
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
+    p.chunk_states = nullptr;  // the end states from zero are not states of the sequence
     int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
     if (rc == GLA_OK) {
         dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
@@ -1164,10 +1182,22 @@ int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *
     if (rc == GLA_OK) {
         p.mode = kSegmented;
         p.grid_seg = nseg;
+        p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
         rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
+}
+
+int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
+                      float *hT, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
+    return chunk_fwd_impl(q, k, v, ld, h0, out, hT, nullptr, nseq, Tlen, H, dk, dv, cu, st);
+}
+
+int tc_chunk_fwd_bf16_save(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
+                           float *hT, void *images, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu,
+                           cudaStream_t st) {
+    return chunk_fwd_impl(q, k, v, ld, h0, out, hT, images, nseq, Tlen, H, dk, dv, cu, st);
 }
 
 // ---- state passes of the backward ------------------------------------------------------

@@ -32,6 +32,9 @@ SIGNATURES = {
     "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_bwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_state_images_bytes": ([_I, _I, _I, _I, _I, _I], ctypes.c_longlong),
+    "gla_chunk_fwd_save": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_bwd_saved": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_decode_step": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_f32": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_paged": ([_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
@@ -213,6 +216,51 @@ def gla_chunk_bwd_f32(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, chunk:
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), nseq, T, H, dk_, dv_, int(chunk),
                                   _ptr(cu_seqlens), _stream(stream))
     _raise(rc, "gla_chunk_bwd_f32")
+
+
+def gla_state_images_bytes(B: int, T: int, H: int, dk: int, dv: int, packed: bool) -> int:
+    """Bytes of the state-image buffer of gla_chunk_fwd_save / gla_chunk_bwd_saved.  See include/gla.h."""
+    return int(load().gla_state_images_bytes(int(B), int(T), int(H), int(dk), int(dv), int(bool(packed))))
+
+
+def state_images(q, v, cu_seqlens=None) -> torch.Tensor:
+    """An uninitialised device buffer for the state images of this batch (bf16, flat)."""
+    B, T, H, dk = q.shape
+    nseq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    n = gla_state_images_bytes(nseq, T, H, dk, v.shape[-1], cu_seqlens is not None)
+    return torch.empty(n // 2, dtype=torch.bfloat16, device=q.device)
+
+
+def _check_images(images, q, v, cu_seqlens):
+    B, T, H, dk = q.shape
+    nseq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    need = gla_state_images_bytes(nseq, T, H, dk, v.shape[-1], cu_seqlens is not None)
+    _check(images, "state_images", torch.bfloat16)
+    if images.numel() * 2 < need:
+        raise ValueError(f"state_images holds {images.numel() * 2} bytes, needs {need}")
+
+
+def gla_chunk_fwd_save(q, k, v, log_decay, h0, out, hT, state_images, chunk: int, cu_seqlens=None,
+                       stream=None) -> None:
+    """gla_chunk_fwd that also writes the state before every chunk to ``state_images`` (for
+    gla_chunk_bwd_saved).  See include/gla.h."""
+    nseq, T, H, dk, dv = _chunk_args(q, k, v, log_decay, h0, out, hT, cu_seqlens, torch.bfloat16)
+    _check_images(state_images, q, v, cu_seqlens)
+    rc = load().gla_chunk_fwd_save(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
+                                   _ptr(state_images), nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens),
+                                   _stream(stream))
+    _raise(rc, "gla_chunk_fwd_save")
+
+
+def gla_chunk_bwd_saved(q, k, v, dout, log_decay, h0, dhT, state_images, dq, dk, dv, dh0, chunk: int,
+                        cu_seqlens=None, stream=None) -> None:
+    """gla_chunk_bwd with the states saved by gla_chunk_fwd_save.  See include/gla.h."""
+    nseq, T, H, dk_, dv_ = _bwd_args(q, k, v, dout, log_decay, h0, dhT, dq, dk, dv, dh0, cu_seqlens, torch.bfloat16)
+    _check_images(state_images, q, v, cu_seqlens)
+    rc = load().gla_chunk_bwd_saved(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(log_decay), _ptr(h0), _ptr(dhT),
+                                    _ptr(state_images), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), nseq, T, H, dk_, dv_,
+                                    int(chunk), _ptr(cu_seqlens), _stream(stream))
+    _raise(rc, "gla_chunk_bwd_saved")
 
 
 def _decode_args(q, k, v, log_decay, state, out, dtype):

@@ -221,6 +221,50 @@ GLA_API int gla_chunk_bwd(const void *q, const void *k, const void *v, const voi
                           int B, int T, int H, int dk, int dv, int chunk, const int32_t *cu_seqlens,
                           void *stream);
 
+/*
+ * Training with saved states.  The tensor-core backward begins by walking
+ * every chain forwards to recover the state before each chunk (it reads k and
+ * v again); the forward already holds that state, as the bf16 tile its
+ * inter-chunk product reads.  gla_chunk_fwd_save is gla_chunk_fwd that also
+ * writes those tiles out, and gla_chunk_bwd_saved is gla_chunk_bwd that takes
+ * them and skips its forward walk.
+ *
+ * gla_state_images_bytes — bytes of the state-image buffer for a batch:
+ *     (rows / 128 + B + 1) * H * dk * dv * 2,   rows = B * T (dense) or T
+ *     (packed: B sequences, T total rows);
+ * chunk c of sequence s (first row start_s) is the dk x dv bf16 tile at slot
+ * start_s / 128 + s + c, the state in force before the chunk (h0, or zeros,
+ * for c = 0), stored in the kernels' shared-memory layout (dv in 64-column
+ * atoms of dk rows x 128 bytes, the 16-byte pieces of row r permuted by
+ * r mod 8): treat it as opaque.  Slots between sequences are never written.
+ * Returns 0 for invalid sizes.
+ */
+GLA_API long long gla_state_images_bytes(int B, int T, int H, int dk, int dv, int packed);
+
+/*
+ * gla_chunk_fwd_save — as gla_chunk_fwd (same arguments, same out and hT)
+ * plus state_images: a device buffer of gla_state_images_bytes(...) bytes,
+ * 16-byte aligned, written as described above.  Only where both the forward
+ * and the backward run on the tensor cores: chunk == 128, 32 | dk <= 128,
+ * 64 | dv <= 192, dv + 2 dk <= 384; otherwise GLA_ERR_UNSUPPORTED (use
+ * gla_chunk_fwd and gla_chunk_bwd).  Extra traffic: 2 dk dv bytes per chunk
+ * and head written.
+ */
+GLA_API int gla_chunk_fwd_save(const void *q, const void *k, const void *v, const float *log_decay,
+                               const float *h0, void *out, float *hT, void *state_images, int B, int T, int H,
+                               int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream);
+
+/*
+ * gla_chunk_bwd_saved — as gla_chunk_bwd, with state_images as written by
+ * gla_chunk_fwd_save for the same q, k, v, log_decay, h0, sizes and
+ * cu_seqlens (read only).  Scratch: one image array (the gradient states)
+ * instead of two.  Same support rule and errors as gla_chunk_fwd_save.
+ */
+GLA_API int gla_chunk_bwd_saved(const void *q, const void *k, const void *v, const void *dout,
+                                const float *log_decay, const float *h0, const float *dhT,
+                                const void *state_images, void *dq, void *dk_out, void *dv_out, float *dh0, int B,
+                                int T, int H, int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream);
+
 /* gla_chunk_bwd_f32 — as gla_chunk_bwd with f32 q, k, v, dout, dq, dk_out, dv_out. */
 GLA_API int gla_chunk_bwd_f32(const float *q, const float *k, const float *v, const float *dout,
                               const float *log_decay, const float *h0, const float *dhT, float *dq,

@@ -93,3 +93,43 @@ def test_two_streams_at_once():
     torch.cuda.synchronize()
     for (o, h), (ro, rh) in zip(outs, refs):
         assert torch.equal(o, ro) and torch.equal(h, rh)
+
+
+def test_saved_states_training_step_in_a_graph():
+    """gla_chunk_fwd_save + gla_chunk_bwd_saved captured once and replayed with new inputs: bit-identical
+    to eager calls (the backward's stream-ordered scratch becomes a graph memory node)."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=640, H=4, h0_std=0.02)
+    bufs = I.make_backward(w, device="cuda", seed=3)
+    out = torch.empty(bufs["q"].shape[:3] + (w.dv,), dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty(2, w.H, w.dk, w.dv, device="cuda")
+    img = gla.state_images(bufs["q"], bufs["v"])
+    dq, dk, dv = (torch.empty_like(bufs[k]) for k in ("q", "k", "v"))
+    dh0 = torch.empty_like(hT)
+
+    def step(b, o, h, im, gq, gk, gv, g0):
+        gla.gla_chunk_fwd_save(b["q"], b["k"], b["v"], b["log_decay"], b["h0"], o, h, im, 128)
+        gla.gla_chunk_bwd_saved(b["q"], b["k"], b["v"], b["dout"], b["log_decay"], b["h0"], b["dhT"], im,
+                                gq, gk, gv, g0, 128)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(bufs, out, hT, img, dq, dk, dv, dh0)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(bufs, out, hT, img, dq, dk, dv, dh0)
+    for seed in (8, 9):
+        d = I.make_backward(w, device="cuda", seed=seed)
+        for k in ("q", "k", "v", "dout", "h0", "dhT"):
+            bufs[k].copy_(d[k])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gla.gla_last_device_status() == 0
+        ref = [torch.empty_like(t) for t in (out, hT, dq, dk, dv, dh0)]
+        img2 = gla.state_images(d["q"], d["v"])
+        step(d, ref[0], ref[1], img2, ref[2], ref[3], ref[4], ref[5])
+        torch.cuda.synchronize()
+        for name, g, r in zip(("out", "hT", "dq", "dk", "dv", "dh0"), (out, hT, dq, dk, dv, dh0), ref):
+            assert torch.equal(g, r), f"{name} differs after replay (seed {seed})"

@@ -110,27 +110,52 @@ constexpr int kLptMaxSeq = 256;
 
 // Shared memory plan (bytes from the 1024-aligned base).
 struct Smem {
-    uint32_t q, k0, k1, v0, v1, s, xp, tab, utab, bars, slot, abort, total;
+    uint32_t q, q1, k0, k1, v0, v1, s, xp, tab, utab, bars, slot, abort, total;
 };
+
+// Barriers, lookup tables and the TMEM slot after the tiles at offset `at`.
+__host__ __device__ inline void smem_plan_tail(Smem &p, uint32_t at) {
+    p.xp = at;                   // output staging: 4 warps x 32 rows x 128 B
+    p.tab = p.xp + 4u * 4096u;
+    p.utab = p.tab + 132 * 4;
+    p.bars = p.utab + 128 * 4;
+    p.bars = (p.bars + 7u) & ~7u;
+    p.slot = p.bars + 32 * 8;  // room for up to 32 barriers
+    p.abort = p.slot + 4;
+    p.total = p.abort + 4;
+}
 
 __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     Smem p;
     const uint32_t qk = (uint32_t)(dk / 32) * 8192u;
     const uint32_t vv = (uint32_t)(dv / 64) * 16384u;
     p.q = 0;
+    p.q1 = p.q;
     p.k0 = p.q + qk;
     p.k1 = p.k0 + qk;
     p.v0 = p.k1 + qk;  // MMA4 reads up to 4 atoms from a K tile: V follows, so the over-read stays in bounds
     p.v1 = p.v0 + vv;
     p.s = p.v1 + vv;
-    p.xp = p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64);  // output staging: 4 warps x 32 rows x 128 B
-    p.tab = p.xp + 4u * 4096u;
-    p.utab = p.tab + 132 * 4;
-    p.bars = p.utab + 128 * 4;
-    p.bars = (p.bars + 7u) & ~7u;
-    p.slot = p.bars + 24 * 8;  // room for up to 24 barriers
-    p.abort = p.slot + 4;
-    p.total = p.abort + 4;
+    smem_plan_tail(p, p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64));
+    return p;
+}
+
+// The full passes (outputs and states): two Q tiles, so that the next chunk's Q is in flight while the
+// current one is still read, and no state-copy tile of its own.  The bf16 copy of S_{c-1} that MMA3(c)
+// reads is written into the V tile of chunk c-1 (free once MMA2(c-1) and MMA4(c-1) are done; dk <= 128
+// rows of dv bf16 fit in its 128 rows), and V(c+1) lands there once MMA3(c) has read it.
+__host__ __device__ inline Smem smem_plan_full(int dk, int dv) {
+    Smem p;
+    const uint32_t qk = (uint32_t)(dk / 32) * 8192u;
+    const uint32_t vv = (uint32_t)(dv / 64) * 16384u;
+    p.q = 0;
+    p.q1 = p.q + qk;
+    p.k0 = p.q1 + qk;
+    p.k1 = p.k0 + qk;
+    p.v0 = p.k1 + qk;  // as above: the over-read of K1 by MMA4 stays inside V0
+    p.v1 = p.v0 + vv;
+    p.s = p.v0;        // no tile of its own (see above)
+    smem_plan_tail(p, p.v1 + vv);
     return p;
 }
 
@@ -138,13 +163,16 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 // Every barrier that can be arrived on for chunk c+1 before its waiter has passed chunk c is kept per
 // K/V stage (KPREP: the K rows of chunk c+1 may be ready before the MMA warp has waited for chunk c's);
 // with parity waits, a barrier must never run two phases ahead of a waiter.
+// In the full passes the K/V barriers of a stage track the K tile alone, and the V tile and the second Q
+// tile have barriers of their own.
 enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP0, B_KPREP1, B_SREADY,
-       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_IMGDONE, B_COUNT };
+       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_IMGDONE,
+       B_QFULL1, B_QEMPTY1, B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1, B_COUNT };
 // barrier of K/V stage s (a state-only pass runs three stages, every other pass two)
 __device__ __forceinline__ int b_kvfull(int s) { return s == 0 ? B_KVFULL0 : s == 1 ? B_KVFULL1 : B_KVFULL2; }
 __device__ __forceinline__ int b_kvempty(int s) { return s == 0 ? B_KVEMPTY0 : s == 1 ? B_KVEMPTY1 : B_KVEMPTY2; }
 __device__ __forceinline__ int b_kprep(int s) { return s == 0 ? B_KPREP0 : s == 1 ? B_KPREP1 : B_KPREP2; }
-static_assert(B_COUNT <= 24, "the shared-memory plan reserves 24 barrier slots");
+static_assert(B_COUNT <= 32, "the shared-memory plan reserves 32 barrier slots");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -179,8 +207,10 @@ __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, fl
 // kRev: the reversed state pass of the backward (kStates with reverse set); a separate instantiation
 // so that the forward's register allocation is untouched.  kNst: K/V stages in flight; the forward's
 // state-only pass has three (its third K tile takes the unused Q buffer, its third V tile the unused
-// state-copy and output-staging space), every other pass two.
-template <bool kRev, int kNst>
+// state-copy and output-staging space), every other pass two.  kFull: the passes that compute outputs
+// (kWhole, kSegmented), with the shared-memory plan of smem_plan_full; the other instances run the
+// state-only modes.
+template <bool kRev, int kNst, bool kFull>
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -190,8 +220,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int dk = P.dk, dv = P.dv, H = P.H;
     const int nka = dk / 32, nva = dv / 64;
     // shared-memory offsets (scalars: nothing of the plan lives in local memory)
-    const Smem plan = smem_plan(dk, dv);
+    const Smem plan = kFull ? smem_plan_full(dk, dv) : smem_plan(dk, dv);
     const uint32_t o_q = plan.q, o_k0 = plan.k0, o_k1 = plan.k1, o_v0 = plan.v0, o_v1 = plan.v1, o_s = plan.s;
+    const uint32_t o_q1 = plan.q1;
     const uint32_t o_xp = plan.xp;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + plan.bars;
@@ -231,11 +262,11 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         __syncthreads();
         seq = lens[P.nseq];
     }
-    const bool state_only = P.mode == kStateOnly || P.mode == kStates;
-    const bool write_images = P.mode == kStates && P.chunk_states != nullptr;
+    const bool state_only = !kFull;
+    const bool write_images = !kFull && P.mode == kStates && P.chunk_states != nullptr;
     // The full forward can also leave the state in force before every chunk, as the bf16 tile MMA3 reads,
     // in the layout the backward consumes (training: the backward then skips its forward state pass).
-    const bool save_images = (P.mode == kWhole || P.mode == kSegmented) && P.chunk_states != nullptr;
+    const bool save_images = kFull && P.chunk_states != nullptr;
     const bool segmented = P.mode == kStateOnly || P.mode == kSegmented || (P.mode == kStates && P.nseg > 1);
 
     SeqRange rng;
@@ -276,15 +307,15 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // the MMAs of consecutive chunks accumulate without a state pass between them, and at the block
     // end one pass scales the state by lambda^(rows of the block).  nblk keeps every frame factor
     // below e^36 (the latest rows, whose weight in the result is about 1, carry the largest).
-    const bool blocked = P.mode == kStateOnly && fact;
+    const bool blocked = !kFull && P.mode == kStateOnly && fact;
     // The backward's state passes (kStates) with a factored decay use the same moving frame; the
     // state before each chunk, for its image, is lambda^(rows walked in the block so far) times the
     // frame, so only the block ends write the state back to TMEM, and the image's copy out of shared
     // memory runs while the next MMA does.
-    const bool framed = P.mode == kStates && fact;
+    const bool framed = !kFull && P.mode == kStates && fact;
     // The backward does not use the state passes' results for strong decays (the chunked SIMT
     // recurrences own those heads, dh0 included), so their CTAs have nothing to do.
-    if (P.mode == kStates && !fact) return;
+    if (!kFull && P.mode == kStates && !fact) return;
     int nblk = 1;
     if (blocked || framed) {
         const float a = -ld * (float)kC;  // >= 0
@@ -301,6 +332,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     auto sph = [&](int c) -> uint32_t { return (uint32_t)(c / kNst) & 1u; };  // its phase on that stage
     auto kbuf_of = [&](int s) -> uint32_t { return s == 0 ? o_k0 : s == 1 ? o_k1 : o_q; };
     auto vbuf_of = [&](int s) -> uint32_t { return s == 0 ? o_v0 : s == 1 ? o_v1 : o_s; };
+    // full passes: Q tile of chunk c, and the state copy S_{c-1} that MMA3(c) reads (in V tile c-1; the
+    // copy of h0 for chunk 0 in the V tile that chunk 1 takes)
+    auto qbuf_of = [&](int c) -> uint32_t { return kFull ? ((c & 1) ? o_q1 : o_q) : o_q; };
+    auto scopy_of = [&](int c) -> uint32_t { return kFull ? ((c & 1) ? o_v0 : o_v1) : o_s; };
 
     if (threadIdx.x == 0) {
         if (!valid) record_status(GLA_ERR_DEVICE_ARG);
@@ -325,6 +360,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_KVEMPTY2), 1);
         mbar_init(BAR(B_KPREP2), 4);
         mbar_init(BAR(B_IMGDONE), 1);
+        mbar_init(BAR(B_QFULL1), 1);
+        mbar_init(BAR(B_QEMPTY1), 1);
+        mbar_init(BAR(B_VFULL0), 1);
+        mbar_init(BAR(B_VFULL1), 1);
+        // a V tile holds a state copy until MMA3 has read it, and, when images are saved, until the
+        // image store has too
+        mbar_init(BAR(B_VEMPTY0), save_images ? 2 : 1);
+        mbar_init(BAR(B_VEMPTY1), save_images ? 2 : 1);
         fence_mbar_init();
     }
     if (threadIdx.x < kC + 4) tab[threadIdx.x] = (threadIdx.x <= kC) ? expf((float)threadIdx.x * ld) : 0.f;
@@ -350,7 +393,27 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint32_t kvbytes = (uint32_t)nka * 8192u + (uint32_t)nva * 16384u;
             const uint32_t qbytes = (uint32_t)nka * 8192u;
             bool ok = true;
-            for (int c = 0; c < nchunks && ok; ++c) {
+            for (int c = 0; c < nchunks && ok && kFull; ++c) {
+                // full passes: Q(c) into its tile once MMA3(c-2) is done, K(c) once MMA4(c-2) is, V(c) once
+                // MMA3(c-1) has read the state copy in its tile (waits in issue order of their releases)
+                const int s = c & 1;
+                const int y = row0 + c * kC;
+                const uint32_t nfree = (uint32_t)((c >> 1) - 1) & 1u;  // phase of the release by chunk c-2
+                const int bqf = s ? B_QFULL1 : B_QFULL, bqe = s ? B_QEMPTY1 : B_QEMPTY;
+                if (c >= 2 && !(ok = mbar_wait(BAR(bqe), nfree, abort_flag, kWaitBudgetNs))) break;
+                mbar_expect_tx(BAR(bqf), qbytes);
+                for (int a = 0; a < nka; ++a) tma_load_2d(sbase + qbuf_of(c) + a * 8192u, &tmQ, h * dk + 32 * a, y, BAR(bqf));
+                if (c >= 2 && !(ok = mbar_wait(BAR(b_kvempty(s)), nfree, abort_flag, kWaitBudgetNs))) break;
+                mbar_expect_tx(BAR(b_kvfull(s)), qbytes);
+                for (int a = 0; a < nka; ++a)
+                    tma_load_2d(sbase + kbuf_of(s) + a * 8192u, &tmK, h * dk + 32 * a, y, BAR(b_kvfull(s)));
+                const int bvf = s ? B_VFULL1 : B_VFULL0, bve = s ? B_VEMPTY1 : B_VEMPTY0;
+                if (c >= 1 && !(ok = mbar_wait(BAR(bve), (uint32_t)((c - 1) >> 1) & 1u, abort_flag, kWaitBudgetNs))) break;
+                mbar_expect_tx(BAR(bvf), kvbytes - qbytes);
+                for (int a = 0; a < nva; ++a)
+                    tma_load_2d(sbase + vbuf_of(s) + a * 16384u, &tmV, h * dv + 64 * a, y, BAR(bvf));
+            }
+            for (int c = 0; c < nchunks && ok && !kFull; ++c) {
                 const int s = stg(c);
                 const int y = row0 + nat(c) * kC;
                 if (c >= kNst) ok = mbar_wait(BAR(b_kvempty(s)), ((c / kNst) - 1) & 1, abort_flag, kWaitBudgetNs);
@@ -380,7 +443,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint32_t id_pv = idesc_bf16(kC, dv, 0, 1);
             const uint32_t id_kv = idesc_bf16(kC, dv, 1, 1);
             const int ksteps_dk = dk / 16;
-            const uint32_t qbuf = sbase + o_q, sbuf = sbase + o_s;
             // image of the state before chunk 0 of this chain (slot start / 128 + seq; chunk c adds c slots)
             // image slot of the state before this segment's first chunk (sequence slot start / 128 + seq,
             // plus the segment's first chunk)
@@ -453,9 +515,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     mma_commit(BAR(b_kvempty(s)));
                     continue;
                 }
-                ok = mbar_wait(BAR(B_KVFULL0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs) &&
-                     mbar_wait(BAR(B_QFULL), c & 1, abort_flag, kWaitBudgetNs) &&
-                     (!fact || mbar_wait(BAR(B_KPREP0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs));
+                // full passes: MMA1(c), MMA3(c), MMA2(c), MMA4(c).  MMA4 last: the state pass of the next
+                // chunk waits for it and then writes its copy into V tile c, which MMA2 has read by then.
+                const uint32_t qbuf = sbase + qbuf_of(c), sbuf = sbase + scopy_of(c);
+                const uint32_t ph = (uint32_t)(c >> 1) & 1u;  // phase of chunk c on its Q tile and K/V stage
+                ok = mbar_wait(BAR(b_kvfull(s)), ph, abort_flag, kWaitBudgetNs) &&
+                     mbar_wait(BAR(s ? B_QFULL1 : B_QFULL), ph, abort_flag, kWaitBudgetNs) &&
+                     (!fact || mbar_wait(BAR(b_kprep(s)), ph, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
                 // MMA1: A = Q K^T, K'' in the factored form (both K-major, 64B swizzle; 2 K-steps per atom)
@@ -471,7 +537,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 if (save_images) {  // the state copy S_{c-1} just written: out to its image slot
-                    bulk_store_s2g(img0 + (int64_t)c * H * sz_state, sbase + o_s, (uint32_t)(sz_state * 2));
+                    bulk_store_s2g(img0 + (int64_t)c * H * sz_state, sbuf, (uint32_t)(sz_state * 2));
                     bulk_commit();
                 }
                 // MMA3: O = Q S_{c-1} (factored) or Q' S_{c-1} (direct); A K-major 64B swizzle,
@@ -482,19 +548,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            smem_desc(sbuf + (uint32_t)kk * 2048u, (uint32_t)dk * 128u, 1024, kSwizzle128B), id_qs,
                            kk > 0);
                 }
-                mma_commit(BAR(B_QEMPTY));  // Q is no longer needed: the next Q may land
-                if (!fact) {
-                    ok = mbar_wait(BAR(B_KPREP0 + s), (c >> 1) & 1, abort_flag, kWaitBudgetNs);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                // MMA4: S += K~^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
-                for (int kk = 0; kk < kC / 16; ++kk) {
-                    mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
-                           smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
-                }
-                mma_commit(BAR(B_SFULL));
-                ok = mbar_wait(BAR(B_PFULL), c & 1, abort_flag, kWaitBudgetNs);
+                mma_commit(BAR(s ? B_QEMPTY1 : B_QEMPTY));    // Q(c+2) may land in this Q tile
+                mma_commit(BAR(s ? B_VEMPTY0 : B_VEMPTY1));   // V(c+1) may land over the copy S_{c-1}
+                ok = mbar_wait(BAR(s ? B_VFULL1 : B_VFULL0), ph, abort_flag, kWaitBudgetNs) &&
+                     mbar_wait(BAR(B_PFULL), c & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 tc_fence_after();
                 // MMA2: O += P V (A = P in TMEM, 8 columns per K-step of 16 tokens)
@@ -503,10 +560,21 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_pv, 1);
                 }
                 mma_commit(BAR(B_OFULL));
-                mma_commit(BAR(B_KVEMPTY0 + s));  // MMA2 and MMA4 were the last readers of this K/V stage
-                if (save_images) {  // the copy may be refilled once the image store has read it
+                if (!fact) {
+                    ok = mbar_wait(BAR(b_kprep(s)), ph, abort_flag, kWaitBudgetNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                // MMA4: S += K~^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
+                for (int kk = 0; kk < kC / 16; ++kk) {
+                    mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
+                           smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
+                }
+                mma_commit(BAR(B_SFULL));        // after MMA2 as well: V tile c may take the next state copy
+                mma_commit(BAR(b_kvempty(s)));   // MMA1 and MMA4 were the readers of this K tile
+                if (save_images) {  // V(c+1) may land once the image store has read the copy
                     bulk_wait_read0();
-                    mbar_arrive(BAR(B_IMGDONE));
+                    mbar_arrive(BAR(s ? B_VEMPTY0 : B_VEMPTY1));
                 }
             }
             if (save_images || write_images) bulk_wait_read0();  // no image store may still read shared memory
@@ -719,8 +787,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (early_k && nchunks > 0) ok = prep_k_early(0);
         for (int c = 0; c <= nchunks && ok; ++c) {
             if (c >= 1) {
-                ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs) &&
-                     (!save_images || mbar_wait(BAR(B_IMGDONE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
+                // (full passes: MMA4(c-1) is issued after MMA2(c-1), so V tile c-1 is free for the copy)
+                ok = mbar_wait(BAR(B_SFULL), (c - 1) & 1, abort_flag, kWaitBudgetNs);
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -767,7 +835,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         continue;
                     }
                     // bf16 copy into the MN-major, 128B-swizzled S tile: one 64-column atom
-                    uint8_t *atom_row = smem + o_s + (uint32_t)(j0 >> 6) * (uint32_t)dk * 128u + (uint32_t)r * 128u;
+                    uint8_t *atom_row = smem + scopy_of(c) + (uint32_t)(j0 >> 6) * (uint32_t)dk * 128u + (uint32_t)r * 128u;
 #pragma unroll
                     for (int q8 = 0; q8 < 8 && (!state_only || write_images); ++q8) {
                         const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
@@ -804,7 +872,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 const int Lc = chunk_len(c);
-                scale_row_sw64(smem + o_q, nka, r, tab[min(r + 1, kC)]);
+                scale_row_sw64(smem + qbuf_of(c), nka, r, tab[min(r + 1, kC)]);
                 fence_async_shared();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(B_QPREP));
@@ -1055,7 +1123,8 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, ui
 bool tc_chunk_supported(int dk, int dv, int chunk) {
     if (!(chunk == kC && dk % 32 == 0 && dk >= 32 && dk <= 128 && dv % 64 == 0 && dv >= 64 && dv <= 192))
         return false;
-    return smem_plan(dk, dv).total + 1024 <= (uint32_t)device_info().max_smem_optin;
+    const uint32_t cap = (uint32_t)device_info().max_smem_optin;
+    return smem_plan(dk, dv).total + 1024 <= cap && smem_plan_full(dk, dv).total + 1024 <= cap;
 }
 
 namespace {
@@ -1085,31 +1154,28 @@ bool three_stages_fit(int dk, int dv) {
     return (uint32_t)(dv / 64) * 16384u <= p.tab - p.s;
 }
 
-int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
-              const Params &p, long long ctas, size_t bytes, cudaStream_t st) {
-    if (ctas <= 0) return GLA_OK;
-    if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    const bool three = p.mode == kStateOnly && three_stages_fit(p.dk, p.dv);
-    if (p.reverse && three) {
-        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes) != cudaSuccess)
-            return GLA_ERR_LAUNCH;
-        gla_tc_chunk_kernel<true, 3><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
-    } else if (p.reverse) {
-        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes) != cudaSuccess)
-            return GLA_ERR_LAUNCH;
-        gla_tc_chunk_kernel<true, 2><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
-    } else if (three) {
-        if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes) != cudaSuccess)
-            return GLA_ERR_LAUNCH;
-        gla_tc_chunk_kernel<false, 3><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
-    } else {
-        gla_tc_chunk_kernel<false, 2><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
-    }
+template <bool kRev, int kNst, bool kFull>
+int launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+               const Params &p, long long ctas, cudaStream_t st) {
+    const size_t bytes = (kFull ? smem_plan_full(p.dk, p.dv) : smem_plan(p.dk, p.dv)).total + 1024;  // + alignment slack
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<kRev, kNst, kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bytes) != cudaSuccess)
+        return GLA_ERR_LAUNCH;
+    gla_tc_chunk_kernel<kRev, kNst, kFull><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
+}
+
+int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+              const Params &p, long long ctas, cudaStream_t st) {
+    if (ctas <= 0) return GLA_OK;
+    if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
+    if (p.mode == kWhole || p.mode == kSegmented) return launch_one<false, 2, true>(mq, mk, mv, mo, p, ctas, st);
+    const bool three = p.mode == kStateOnly && three_stages_fit(p.dk, p.dv);
+    if (p.reverse && three) return launch_one<true, 3, false>(mq, mk, mv, mo, p, ctas, st);
+    if (p.reverse) return launch_one<true, 2, false>(mq, mk, mv, mo, p, ctas, st);
+    if (three) return launch_one<false, 3, false>(mq, mk, mv, mo, p, ctas, st);
+    return launch_one<false, 2, false>(mq, mk, mv, mo, p, ctas, st);
 }
 
 }  // namespace
@@ -1127,11 +1193,6 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
-        return GLA_ERR_LAUNCH;
-    const Smem sp = smem_plan(dk, dv);
-    const size_t bytes = sp.total + 1024;  // + alignment slack
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-        cudaSuccess)
         return GLA_ERR_LAUNCH;
     Params p{};
     p.log_decay = ld;
@@ -1155,7 +1216,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
     p.lpt = (cu != nullptr && nseg == 1 && nseq > 1 && nseq <= kLptMaxSeq) ? 1 : 0;
-    if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, bytes, st);
+    if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, st);
 
     // segmented schedule: stream-ordered scratch for the segment end / start states
     const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
@@ -1171,7 +1232,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
     p.chunk_states = nullptr;  // the end states from zero are not states of the sequence
-    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), st);
     if (rc == GLA_OK) {
         dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
         gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg,
@@ -1183,7 +1244,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
         p.mode = kSegmented;
         p.grid_seg = nseg;
         p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
-        rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
+        rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
@@ -1217,10 +1278,6 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     if (!make_map(&mk, ka, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mv, va, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return GLA_ERR_LAUNCH;
-    const size_t bytes = smem_plan(dk, dv).total + 1024;
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-        cudaSuccess)
-        return GLA_ERR_LAUNCH;
     Params p{};
     p.log_decay = ld;
     p.h0 = init;
@@ -1241,7 +1298,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
     p.lpt = (cu != nullptr && nseg == 1 && nseq > 1 && nseq <= kLptMaxSeq) ? 1 : 0;
     // the q and out maps are not read in a state-only pass
-    if (nseg == 1) return launch_tc(mk, mk, mv, mv, p, chains, bytes, st);
+    if (nseg == 1) return launch_tc(mk, mk, mv, mv, p, chains, st);
 
     // few long chains: as the forward's segmented schedule, in walk order (backwards in time the first
     // walked segment is the sequence's last, which may be short): end states of walk segments
@@ -1258,7 +1315,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     p.seg_h0 = scratch + per;
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mk, mk, mv, mv, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mk, mk, mv, mv, p, chains * (nseg - 1), st);
     if (rc == GLA_OK) {
         const int seg_tokens = seg_chunks * kC;
         const int first_tokens = reverse ? Tlen - (nseg - 1) * seg_tokens : seg_tokens;
@@ -1271,7 +1328,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     if (rc == GLA_OK) {
         p.mode = kStates;
         p.grid_seg = nseg;
-        rc = launch_tc(mk, mk, mv, mv, p, chains * nseg, bytes, st);
+        rc = launch_tc(mk, mk, mv, mv, p, chains * nseg, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
@@ -1334,10 +1391,6 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
         !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
         return GLA_ERR_LAUNCH;
-    const size_t bytes = smem_plan(dk, dv).total + 1024;
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-        cudaSuccess)
-        return GLA_ERR_LAUNCH;
     Params p{};
     p.log_decay = ld;
     p.h0 = h0;
@@ -1354,7 +1407,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     p.seg_h0 = scratch + per;   // written in full by the scan before pass 2 reads it
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), bytes, st);
+    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), st);
     if (rc != GLA_OK) return rc;
     dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
     gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC,
@@ -1363,7 +1416,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     p.mode = kSegmented;
     p.grid_seg = nseg;
-    return launch_tc(mq, mk, mv, mo, p, chains * nseg, bytes, st);
+    return launch_tc(mq, mk, mv, mo, p, chains * nseg, st);
 }
 
 }  // namespace gla

@@ -165,8 +165,8 @@ __host__ __device__ inline Smem smem_plan_full(int dk, int dv) {
 // with parity waits, a barrier must never run two phases ahead of a waiter.
 // In the full passes the K/V barriers of a stage track the K tile alone, and the V tile and the second Q
 // tile have barriers of their own.
-enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_QPREP, B_KPREP0, B_KPREP1, B_SREADY,
-       B_PFULL, B_OFULL, B_OFREE, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_IMGDONE,
+enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AFULL, B_KPREP0, B_KPREP1, B_SREADY,
+       B_PFULL, B_OFULL, B_SFULL, B_FINAL, B_KVFULL2, B_KVEMPTY2, B_KPREP2, B_IMGDONE,
        B_QFULL1, B_QEMPTY1, B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1, B_COUNT };
 // barrier of K/V stage s (a state-only pass runs three stages, every other pass two)
 __device__ __forceinline__ int b_kvfull(int s) { return s == 0 ? B_KVFULL0 : s == 1 ? B_KVFULL1 : B_KVFULL2; }
@@ -347,13 +347,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_init(BAR(B_KVEMPTY0), 1);
         mbar_init(BAR(B_KVEMPTY1), 1);
         mbar_init(BAR(B_AFULL), 1);
-        mbar_init(BAR(B_QPREP), 4);
         mbar_init(BAR(B_KPREP0), 4);
         mbar_init(BAR(B_KPREP1), 4);
-        mbar_init(BAR(B_SREADY), 4);
+        // full passes: the state warps' copy (and, direct form, Q prep) plus the epilogue warps' release
+        // of O, so that MMA3 waits on one barrier
+        mbar_init(BAR(B_SREADY), kFull ? 8 : 4);
         mbar_init(BAR(B_PFULL), 4);
         mbar_init(BAR(B_OFULL), 1);
-        mbar_init(BAR(B_OFREE), 4);
         mbar_init(BAR(B_SFULL), 1);
         mbar_init(BAR(B_FINAL), 1);
         mbar_init(BAR(B_KVFULL2), 1);
@@ -519,9 +519,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 // chunk waits for it and then writes its copy into V tile c, which MMA2 has read by then.
                 const uint32_t qbuf = sbase + qbuf_of(c), sbuf = sbase + scopy_of(c);
                 const uint32_t ph = (uint32_t)(c >> 1) & 1u;  // phase of chunk c on its Q tile and K/V stage
-                ok = mbar_wait(BAR(b_kvfull(s)), ph, abort_flag, kWaitBudgetNs) &&
-                     mbar_wait(BAR(s ? B_QFULL1 : B_QFULL), ph, abort_flag, kWaitBudgetNs) &&
-                     (!fact || mbar_wait(BAR(b_kprep(s)), ph, abort_flag, kWaitBudgetNs));
+                // (factored form: KPREP implies that K has landed)
+                ok = mbar_wait(BAR(s ? B_QFULL1 : B_QFULL), ph, abort_flag, kWaitBudgetNs) &&
+                     (fact ? mbar_wait(BAR(b_kprep(s)), ph, abort_flag, kWaitBudgetNs)
+                           : mbar_wait(BAR(b_kvfull(s)), ph, abort_flag, kWaitBudgetNs));
                 if (!ok) break;
                 tc_fence_after();
                 // MMA1: A = Q K^T, K'' in the factored form (both K-major, 64B swizzle; 2 K-steps per atom)
@@ -531,9 +532,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                            smem_desc(kbuf + off, 16, 512, kSwizzle64B), id_qk, kk > 0);
                 }
                 mma_commit(BAR(B_AFULL));
-                ok = (fact || mbar_wait(BAR(B_QPREP), c & 1, abort_flag, kWaitBudgetNs)) &&
-                     mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs) &&
-                     (c == 0 || mbar_wait(BAR(B_OFREE), (c - 1) & 1, abort_flag, kWaitBudgetNs));
+                ok = mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);  // copy S_{c-1} ready, O free
                 if (!ok) break;
                 tc_fence_after();
                 if (save_images) {  // the state copy S_{c-1} just written: out to its image slot
@@ -862,7 +861,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             fence_async_shared();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SREADY));
+            if (lane == 0 && early_k) mbar_arrive(BAR(B_SREADY));  // (direct form: after the Q prep below)
 
             if (early_k) {
                 if (c + 1 < nchunks) ok = prep_k_early(c + 1);
@@ -875,7 +874,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 scale_row_sw64(smem + qbuf_of(c), nka, r, tab[min(r + 1, kC)]);
                 fence_async_shared();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(B_QPREP));
+                if (lane == 0) mbar_arrive(BAR(B_SREADY));  // the state copy and Q' are ready for MMA3
                 scale_row_sw64(smem + ((c & 1) ? o_k1 : o_k0), nka, r, (r < Lc) ? tab[Lc - 1 - r] : 0.f);
                 fence_async_shared();
                 __syncwarp();
@@ -958,6 +957,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
         uint8_t *xp = smem + o_xp + (uint32_t)q4 * 4096u;     // this warp's staging tile: 32 rows x 128 B
         bool ok = true;
+        // O is free for the first chunk's MMA3 (the releases of O count toward SREADY, one phase later)
+        if (!state_only && nchunks > 0 && lane == 0) mbar_arrive(BAR(B_SREADY));
         for (int c = 0; c < nchunks && ok && !state_only; ++c) {
             const int Lc = chunk_len(c);
             // ---- output epilogue: O -> bf16 rows in this warp's 4 KB staging tile (one 64-column
@@ -976,7 +977,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (j0 + 64 >= dv) {  // last TMEM read of O for this chunk: MMA3 of the next chunk may start
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(B_OFREE));
+                    if (lane == 0) mbar_arrive(BAR(B_SREADY));
                 }
                 if (lane == 0) bulk_wait_read0();  // the previous store out of the staging tile has read it
                 __syncwarp();

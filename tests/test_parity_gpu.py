@@ -85,10 +85,23 @@ def test_bf16_layer_shapes_small(chunk):
 
 
 @pytest.mark.parametrize("dk,dv", [(32, 64), (64, 64), (64, 128), (128, 192), (96, 128), (128, 64),
-                                   (48, 80), (16, 16), (256, 64)])
+                                   (128, 128), (32, 192), (48, 80), (16, 16), (256, 64)])
 def test_bf16_other_head_sizes(dk, dv):
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=260, H=2, dk=dk, dv=dv, h0_std=0.1)
     check_prefill(w, chunk=128, seed=3)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (32, 192)])
+def test_bf16_direct_decay_form_head_sizes(dk, dv):
+    """The direct decay form (lambda < e^-0.3: Q and K rows decayed in place after MMA1, per-element decay
+    in the mask) with other tile sizes, a ragged tail and an initial state."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=390, H=2, dk=dk, dv=dv, h0_std=0.1)
+    d = with_dev_cu(I.make_prefill(w, device="cuda", seed=14))
+    d["log_decay"] = torch.tensor([-0.45, -1.7], device="cuda")
+    out, hT = run_prefill(d, 128)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(out.float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
 
 
 @pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 256, 385])

@@ -65,6 +65,8 @@ def _load():
             lib.gla_oracle_backward.restype = I
             lib.gla_oracle_conv1d_silu.argtypes = [P] * 8 + [I, I]
             lib.gla_oracle_conv1d_silu.restype = I
+            lib.gla_oracle_output_gate.argtypes = [P, P, I, P, ctypes.c_int64]
+            lib.gla_oracle_output_gate.restype = I
             _lib = lib
     return _lib
 
@@ -243,6 +245,24 @@ def decode_step(q, k, v, log_decay, state, nthreads=None):
     if rc != 0:
         raise ValueError("oracle decode rejected its arguments")
     return o, st
+
+
+GATE_SILU, GATE_SIGMOID = 0, 1
+
+
+def output_gate(o, g, kind=GATE_SILU):
+    """The mixer output times a function of the gate g_t ([L3B] "i14 与 Laplace 3B 架构", QKVG
+    projection: the gate acts after the mixer).  kind 0: o * g / (1 + exp(-g)) (SiLU), kind 1:
+    o / (1 + exp(-g)) (sigmoid).  o and g have the same shape; returns float64."""
+    o = _f64(o)
+    g = _f32(g)
+    if o.shape != g.shape:
+        raise ValueError("o and g must have the same shape")
+    out = np.empty_like(o)
+    rc = _load().gla_oracle_output_gate(_ptr(o), _ptr(g), int(kind), _ptr(out), o.size)
+    if rc != 0:
+        raise ValueError("oracle output gate rejected its arguments")
+    return out
 
 
 def rel_err(got, ref) -> float:

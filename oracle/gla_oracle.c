@@ -499,3 +499,23 @@ int gla_oracle_conv1d_silu(const float *x, const double *w, const double *b, con
     }
     return 0;
 }
+
+/*
+ * Output gate ([L3B] §"i14 与 Laplace 3B 架构", "QKVG 投影": the fused projection
+ * splits into q_t, k_t, v_t and a gate g_t of H x dv values per token, and the
+ * gate acts after the mixer).  The page names the gate and where it acts but
+ * prints no formula; the reading taken here is an elementwise product of the
+ * mixer output o_t with a function of g_t:
+ *   kind 0:  o'_t = o_t * g_t / (1 + exp(-g_t))      (swish / SiLU gate)
+ *   kind 1:  o'_t = o_t * 1 / (1 + exp(-g_t))        (sigmoid gate)
+ *   o, out : n float64 values (out may be o);  g : n float32 values
+ */
+int gla_oracle_output_gate(const double *o, const float *g, int kind, double *out, int64_t n) {
+    if (!o || !g || !out || n < 0 || (kind != 0 && kind != 1)) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const double x = (double)g[i];
+        const double sig = 1.0 / (1.0 + exp(-x));
+        out[i] = o[i] * (kind == 0 ? x * sig : sig);
+    }
+    return 0;
+}

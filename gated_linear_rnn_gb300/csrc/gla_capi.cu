@@ -48,6 +48,13 @@ int conv1d_silu_f32(const float *, const float *, const float *, const float *, 
 int conv1d_silu_step_bf16(const void *, const float *, const float *, float *, void *, int, int, cudaStream_t);
 int chunk_fwd_host_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *,
                         int, int, int, int, int, int, cudaStream_t);
+int tc_chunk_fwd_gated_bf16(const void *, const void *, const void *, const void *, int, const float *, const float *,
+                            void *, float *, int, int, int, int, int, const int32_t *, cudaStream_t);
+int simt_chunk_fwd_gated_bf16(const void *, const void *, const void *, const void *, int, const float *,
+                              const float *, void *, float *, int, int, int, int, int, int, const int32_t *,
+                              cudaStream_t);
+int decode_step_gated_bf16(const void *, const void *, const void *, const void *, int, const float *, float *,
+                           const int32_t *, int, void *, int, int, int, int, cudaStream_t);
 int take_status_conv(cudaStream_t);
 int take_status_simt(cudaStream_t);
 int take_status_bwd(cudaStream_t);
@@ -153,6 +160,22 @@ int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
         return tc_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens, st);
     return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
+}
+
+int gla_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                        const float *log_decay, const float *h0, void *out, float *hT, int B, int T, int H, int dk,
+                        int dv, int chunk, const int32_t *cu_seqlens, void *stream) {
+    if (!g) return GLA_ERR_ARG;
+    if (gate_kind != GLA_GATE_SILU && gate_kind != GLA_GATE_SIGMOID) return GLA_ERR_ARG;
+    int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
+    if (rc) return rc;
+    if (!aligned16(g)) return GLA_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+        return tc_chunk_fwd_gated_bf16(q, k, v, g, gate_kind, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens,
+                                       st);
+    return simt_chunk_fwd_gated_bf16(q, k, v, g, gate_kind, log_decay, h0, out, hT, B, T, H, dk, dv, chunk,
+                                     cu_seqlens, st);
 }
 
 int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_decay, const float *h0,
@@ -263,6 +286,31 @@ int gla_decode_step_paged(const void *q, const void *k, const void *v, const flo
     if (!aligned16(slots)) return GLA_ERR_ALIGN;
     if ((long long)nslots * H > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     return decode_step_paged_bf16(q, k, v, log_decay, state_pool, slots, nslots, out, N, H, dk, dv,
+                                  (cudaStream_t)stream);
+}
+
+int gla_decode_step_gated(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                          const float *log_decay, float *state_inout, void *out, int N, int H, int dk, int dv,
+                          void *stream) {
+    if (!g) return GLA_ERR_ARG;
+    if (gate_kind != GLA_GATE_SILU && gate_kind != GLA_GATE_SIGMOID) return GLA_ERR_ARG;
+    int rc = check_decode(q, k, v, log_decay, state_inout, out, N, H, dk, dv);
+    if (rc) return rc;
+    if (!aligned16(g)) return GLA_ERR_ALIGN;
+    return decode_step_gated_bf16(q, k, v, g, gate_kind, log_decay, state_inout, nullptr, 0, out, N, H, dk, dv,
+                                  (cudaStream_t)stream);
+}
+
+int gla_decode_step_paged_gated(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                                const float *log_decay, float *state_pool, const int32_t *slots, int nslots,
+                                void *out, int N, int H, int dk, int dv, void *stream) {
+    if (!g || !slots || nslots <= 0) return GLA_ERR_ARG;
+    if (gate_kind != GLA_GATE_SILU && gate_kind != GLA_GATE_SIGMOID) return GLA_ERR_ARG;
+    int rc = check_decode(q, k, v, log_decay, state_pool, out, N, H, dk, dv);
+    if (rc) return rc;
+    if (!aligned16(g) || !aligned16(slots)) return GLA_ERR_ALIGN;
+    if ((long long)nslots * H > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
+    return decode_step_gated_bf16(q, k, v, g, gate_kind, log_decay, state_pool, slots, nslots, out, N, H, dk, dv,
                                   (cudaStream_t)stream);
 }
 

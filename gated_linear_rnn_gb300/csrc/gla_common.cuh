@@ -20,6 +20,14 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Output gate factor (the gate g_t of the QKVG projection acts on the mixer output): kind 0 multiplies
+// by SiLU(g) = g / (1 + e^-g), kind 1 by the sigmoid 1 / (1 + e^-g).  For g below about -87 the
+// exponential overflows to +inf and the reciprocal to 0, which is the limit.
+__device__ __forceinline__ float gate_factor(float g, int kind) {
+    const float sig = __fdividef(1.f, 1.f + __expf(-g));
+    return kind == 0 ? g * sig : sig;
+}
+
 // ---- chain bookkeeping ---------------------------------------------------
 // A chain is one (sequence, head) pair.  Dense batches: sequence s covers rows
 // s*T .. s*T+T-1.  Packed batches: rows cu[s] .. cu[s+1]-1.  Returns false (and

@@ -54,7 +54,8 @@ template <typename T, int kMaxThreads, int kUnroll>
 __global__ void __launch_bounds__(kMaxThreads)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ log_decay, float *__restrict__ state, T *__restrict__ out,
-              int H, int dk, int dv, const int32_t *__restrict__ slots, int nslots) {
+              int H, int dk, int dv, const int32_t *__restrict__ slots, int nslots, const T *__restrict__ gate,
+              int gate_kind) {
     extern __shared__ float sm[];
     float *qs = sm, *ks = sm + dk, *red = sm + 2 * dk;  // red: [kRG][dv]
     const int unit = blockIdx.x;                          // n * H + h
@@ -124,13 +125,15 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
         float o = 0.f;
 #pragma unroll
         for (int g = 0; g < kRG; ++g) o += red[g * dv + c];
+        if (gate != nullptr) o *= gate_factor(to_f32(gate[(size_t)unit * dv + c]), gate_kind);
         out[(size_t)unit * dv + c] = from_f32<T>(o);
     }
 }
 
 template <typename T>
 int launch_decode(const T *q, const T *k, const T *v, const float *ld, float *state, T *out, int N, int H,
-                  int dk, int dv, cudaStream_t st, const int32_t *slots = nullptr, int nslots = 0) {
+                  int dk, int dv, cudaStream_t st, const int32_t *slots = nullptr, int nslots = 0,
+                  const T *gate = nullptr, int gate_kind = 0) {
     const long long units = (long long)N * H;
     if (units > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     const int threads = (dv / 4) * kRG;
@@ -138,10 +141,10 @@ int launch_decode(const T *q, const T *k, const T *v, const float *ld, float *st
     const size_t bytes = (size_t)(2 * dk + kRG * dv) * sizeof(float);
     if (threads <= 256)
         decode_kernel<T, 256, 12><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv,
-                                                                           slots, nslots);
+                                                                           slots, nslots, gate, gate_kind);
     else
         decode_kernel<T, 1024, 4><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv,
-                                                                           slots, nslots);
+                                                                           slots, nslots, gate, gate_kind);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -165,6 +168,15 @@ int decode_step_paged_bf16(const void *q, const void *k, const void *v, const fl
     using B = __nv_bfloat16;
     return launch_decode<B>((const B *)q, (const B *)k, (const B *)v, ld, pool, (B *)out, N, H, dk, dv, st, slots,
                             nslots);
+}
+
+// The step with the output gate applied to o (slots null: the dense state layout).
+int decode_step_gated_bf16(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                           const float *ld, float *state, const int32_t *slots, int nslots, void *out, int N, int H,
+                           int dk, int dv, cudaStream_t st) {
+    using B = __nv_bfloat16;
+    return launch_decode<B>((const B *)q, (const B *)k, (const B *)v, ld, state, (B *)out, N, H, dk, dv, st, slots,
+                            nslots, (const B *)g, gate_kind);
 }
 
 }  // namespace gla

@@ -69,7 +69,8 @@ __global__ void __launch_bounds__(kThreads)
 simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                   const float *__restrict__ log_decay, const float *__restrict__ h0,
                   T *__restrict__ out, float *__restrict__ hT, int nseq, int Tlen, int H, int dk,
-                  int dv, int dvt, const int32_t *__restrict__ cu, int state_mode) {
+                  int dv, int dvt, const int32_t *__restrict__ cu, int state_mode, const T *__restrict__ gate,
+                  int gate_kind) {
     extern __shared__ float smem[];
     const SimtSmem Lo = simt_layout(C, dk, dvt);
     float *Qs = smem + Lo.q, *Ks = smem + Lo.k, *Vs = smem + Lo.vv, *As = smem + Lo.a;
@@ -189,11 +190,16 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
                 const int i = bi * 4 + a;
                 if (i >= L) continue;
                 const float g = tab[i + 1 - sh];
-                T *orow = out + ((size_t)row_of(c0, i) * H + h) * dv + j0;
+                const size_t ro = ((size_t)row_of(c0, i) * H + h) * dv + j0;
+                T *orow = out + ro;
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     const int c = bc * 4 + b;
-                    if (c < nc) orow[c] = from_f32<T>(fmaf(g, inter[a][b], intra[a][b]));
+                    if (c < nc) {
+                        float o = fmaf(g, inter[a][b], intra[a][b]);
+                        if (gate != nullptr) o *= gate_factor(to_f32(gate[ro + c]), gate_kind);
+                        orow[c] = from_f32<T>(o);
+                    }
                 }
             }
         }
@@ -237,7 +243,8 @@ simt_chunk_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
 
 template <typename T, int C, bool Rev>
 int launch_c(const T *q, const T *k, const T *v, const float *ld, const float *h0, T *out, float *hT,
-             int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, int state_mode, cudaStream_t st) {
+             int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, int state_mode, cudaStream_t st,
+             const T *gate, int gate_kind) {
     const DeviceInfo &di = device_info();
     const size_t limit = std::min<size_t>((size_t)di.max_smem_optin, 200 * 1024);
     int dvt = 64;
@@ -256,7 +263,8 @@ int launch_c(const T *q, const T *k, const T *v, const float *ld, const float *h
     const int tiles = (dv + dvt - 1) / dvt;
     if (chains > 0x7fffffffLL || tiles > 65535) return GLA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)chains, (unsigned)tiles);
-    kern<<<grid, kThreads, bytes, st>>>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, dvt, cu, state_mode);
+    kern<<<grid, kThreads, bytes, st>>>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, dvt, cu, state_mode, gate,
+                                        gate_kind);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -264,17 +272,17 @@ int launch_c(const T *q, const T *k, const T *v, const float *ld, const float *h
 template <typename T, bool Rev = false>
 int launch_simt(const T *q, const T *k, const T *v, const float *ld, const float *h0, T *out, float *hT,
                 int nseq, int Tlen, int H, int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st,
-                int state_mode = 0) {
+                int state_mode = 0, const T *gate = nullptr, int gate_kind = 0) {
     if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return GLA_ERR_UNSUPPORTED;
     // A chunk whose tiles do not fit in shared memory is processed as sub-chunks
     // of half the length (the chunked form is the same map for any chunk length).
     int rc = GLA_ERR_UNSUPPORTED;
     for (int c = chunk; c >= 16 && rc == GLA_ERR_UNSUPPORTED; c /= 2) {
         switch (c) {
-            case 16: rc = launch_c<T, 16, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
-            case 32: rc = launch_c<T, 32, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
-            case 64: rc = launch_c<T, 64, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
-            default: rc = launch_c<T, 128, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st); break;
+            case 16: rc = launch_c<T, 16, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st, gate, gate_kind); break;
+            case 32: rc = launch_c<T, 32, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st, gate, gate_kind); break;
+            case 64: rc = launch_c<T, 64, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st, gate, gate_kind); break;
+            default: rc = launch_c<T, 128, Rev>(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, state_mode, st, gate, gate_kind); break;
         }
     }
     return rc;
@@ -294,6 +302,15 @@ int simt_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float
     using B = __nv_bfloat16;
     return launch_simt<B>((const B *)q, (const B *)k, (const B *)v, ld, h0, (B *)out, hT, nseq, Tlen, H, dk,
                           dv, chunk, cu, st);
+}
+
+// The same forward with the output gate applied to every output row (gate: [rows, H, dv] like out).
+int simt_chunk_fwd_gated_bf16(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                              const float *ld, const float *h0, void *out, float *hT, int nseq, int Tlen, int H,
+                              int dk, int dv, int chunk, const int32_t *cu, cudaStream_t st) {
+    using B = __nv_bfloat16;
+    return launch_simt<B>((const B *)q, (const B *)k, (const B *)v, ld, h0, (B *)out, hT, nseq, Tlen, H, dk,
+                          dv, chunk, cu, st, 0, (const B *)g, gate_kind);
 }
 
 // Backward of the chunked forward: three recurrences (see the top of this file), each a launch of

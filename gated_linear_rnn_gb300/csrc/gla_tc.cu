@@ -102,6 +102,8 @@ struct Params {
                                   // slot start_s / 128 + s + c (start_s its first row)
     int nseq;              // sequences (packed batches: entries of cu minus one)
     int lpt;               // packed batch, whole chains: CTA i takes the sequence of length rank i / H
+    const __nv_bfloat16 *gate;  // full passes with the output gate: [rows, H, dv] like out (kGate instance)
+    int gate_kind;              // 0: out = O * SiLU(g); 1: out = O * sigmoid(g)
 };
 
 // Packed batches of up to this many sequences are walked longest first (the ranking costs every CTA
@@ -209,8 +211,8 @@ __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, fl
 // state-only pass has three (its third K tile takes the unused Q buffer, its third V tile the unused
 // state-copy and output-staging space), every other pass two.  kFull: the passes that compute outputs
 // (kWhole, kSegmented), with the shared-memory plan of smem_plan_full; the other instances run the
-// state-only modes.
-template <bool kRev, int kNst, bool kFull>
+// state-only modes.  kGate: a full pass that multiplies every output by the output gate's factor.
+template <bool kRev, int kNst, bool kFull, bool kGate = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -971,6 +973,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const bool full = (Lc == kC);
             for (int j0 = 0; j0 < dv; j0 += 64) {
                 uint32_t v[2][32];
+                // output gate of this row's 64 columns (8 x 8 bf16), in flight with the TMEM loads
+                uint4 gv[kGate ? 8 : 1];
+                if (kGate) {
+                    const uint4 *gp = reinterpret_cast<const uint4 *>(P.gate + ((row0 + (int64_t)c * kC + r) * H + h) * dv + j0);
+#pragma unroll
+                    for (int i = 0; i < (kGate ? 8 : 1); ++i) gv[i] = (r < Lc) ? __ldg(gp + i) : make_uint4(0u, 0u, 0u, 0u);
+                }
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0 + 32u, v[1]);
                 tmem_wait_ld();
@@ -985,7 +994,17 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 uint8_t *myrow = xp + (uint32_t)lane * 128u;
 #pragma unroll
                 for (int q8 = 0; q8 < 8; ++q8) {
-                    const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                    uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                    if (kGate) {
+                        const uint32_t gw[4] = {gv[kGate ? q8 : 0].x, gv[kGate ? q8 : 0].y, gv[kGate ? q8 : 0].z,
+                                                gv[kGate ? q8 : 0].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[e]));
+                            x[2 * e] = __float_as_uint(__uint_as_float(x[2 * e]) * gate_factor(gf.x, P.gate_kind));
+                            x[2 * e + 1] = __float_as_uint(__uint_as_float(x[2 * e + 1]) * gate_factor(gf.y, P.gate_kind));
+                        }
+                    }
                     *reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4)) = make_uint4(
                         pack_bf16x2(__uint_as_float(x[0]) * grow, __uint_as_float(x[1]) * grow),
                         pack_bf16x2(__uint_as_float(x[2]) * grow, __uint_as_float(x[3]) * grow),
@@ -1155,14 +1174,14 @@ bool three_stages_fit(int dk, int dv) {
     return (uint32_t)(dv / 64) * 16384u <= p.tab - p.s;
 }
 
-template <bool kRev, int kNst, bool kFull>
+template <bool kRev, int kNst, bool kFull, bool kGate = false>
 int launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                const Params &p, long long ctas, cudaStream_t st) {
     const size_t bytes = (kFull ? smem_plan_full(p.dk, p.dv) : smem_plan(p.dk, p.dv)).total + 1024;  // + alignment slack
-    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<kRev, kNst, kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gla_tc_chunk_kernel<kRev, kNst, kFull, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bytes) != cudaSuccess)
         return GLA_ERR_LAUNCH;
-    gla_tc_chunk_kernel<kRev, kNst, kFull><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    gla_tc_chunk_kernel<kRev, kNst, kFull, kGate><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -1171,7 +1190,9 @@ int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &m
               const Params &p, long long ctas, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
-    if (p.mode == kWhole || p.mode == kSegmented) return launch_one<false, 2, true>(mq, mk, mv, mo, p, ctas, st);
+    if (p.mode == kWhole || p.mode == kSegmented)
+        return p.gate ? launch_one<false, 2, true, true>(mq, mk, mv, mo, p, ctas, st)
+                      : launch_one<false, 2, true, false>(mq, mk, mv, mo, p, ctas, st);
     const bool three = p.mode == kStateOnly && three_stages_fit(p.dk, p.dv);
     if (p.reverse && three) return launch_one<true, 3, false>(mq, mk, mv, mo, p, ctas, st);
     if (p.reverse) return launch_one<true, 2, false>(mq, mk, mv, mo, p, ctas, st);
@@ -1185,7 +1206,7 @@ int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &m
 // force before every chunk there ([slots, H, dk, dv], chunk c of sequence s at slot start_s / 128 + s + c).
 static int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
                    float *hT, void *images, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu,
-                   cudaStream_t st) {
+                   cudaStream_t st, const void *gate = nullptr, int gate_kind = 0) {
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
@@ -1213,6 +1234,8 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     p.seg_end = nullptr;
     p.nseq = nseq;
     p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
+    p.gate = reinterpret_cast<const __nv_bfloat16 *>(gate);
+    p.gate_kind = gate_kind;
     const long long chains = (long long)nseq * H;
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
@@ -1254,6 +1277,13 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
 int tc_chunk_fwd_bf16(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,
                       float *hT, int nseq, int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
     return chunk_fwd_impl(q, k, v, ld, h0, out, hT, nullptr, nseq, Tlen, H, dk, dv, cu, st);
+}
+
+// The forward with the output gate applied to every output row (gate: [rows, H, dv] like out).
+int tc_chunk_fwd_gated_bf16(const void *q, const void *k, const void *v, const void *g, int gate_kind, const float *ld,
+                            const float *h0, void *out, float *hT, int nseq, int Tlen, int H, int dk, int dv,
+                            const int32_t *cu, cudaStream_t st) {
+    return chunk_fwd_impl(q, k, v, ld, h0, out, hT, nullptr, nseq, Tlen, H, dk, dv, cu, st, g, gate_kind);
 }
 
 int tc_chunk_fwd_bf16_save(const void *q, const void *k, const void *v, const float *ld, const float *h0, void *out,

@@ -27,6 +27,9 @@ STATUS = {0: "GLA_OK", -1: "GLA_ERR_ARG", -2: "GLA_ERR_UNSUPPORTED", -3: "GLA_ER
 _P, _I = ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "gla_chunk_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_chunk_fwd_gated": ([_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "gla_decode_step_gated": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "gla_decode_step_paged_gated": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
     "gla_chunk_fwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_fwd_host": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
@@ -143,6 +146,21 @@ def gla_chunk_fwd(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, 
     rc = load().gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(h0), _ptr(out), _ptr(hT),
                               nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens), _stream(stream))
     _raise(rc, "gla_chunk_fwd")
+
+
+GATE_SILU, GATE_SIGMOID = 0, 1  # gla_gate_kind
+
+
+def gla_chunk_fwd_gated(q, k, v, g, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, gate_kind: int = GATE_SILU,
+                        stream=None) -> None:
+    """bf16 chunked forward with the output gate fused into the write of ``out``: out = o * f(g), f = SiLU
+    (gate_kind 0) or sigmoid (1); ``g`` has the shape of ``out``.  See include/gla.h."""
+    nseq, T, H, dk, dv = _chunk_args(q, k, v, log_decay, h0, out, hT, cu_seqlens, torch.bfloat16)
+    _check(g, "g", torch.bfloat16, tuple(out.shape))
+    rc = load().gla_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), int(gate_kind), _ptr(log_decay), _ptr(h0),
+                                    _ptr(out), _ptr(hT), nseq, T, H, dk, dv, int(chunk), _ptr(cu_seqlens),
+                                    _stream(stream))
+    _raise(rc, "gla_chunk_fwd_gated")
 
 
 def gla_chunk_fwd_noalloc(q, k, v, log_decay, h0, out, hT, chunk: int, cu_seqlens=None, stream=None) -> None:
@@ -308,6 +326,36 @@ def gla_decode_step_paged(q, k, v, log_decay, state_pool, slots, out, stream=Non
     rc = load().gla_decode_step_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(log_decay), _ptr(state_pool), _ptr(slots),
                                       int(state_pool.shape[0]), _ptr(out), N, H, dk, dv, _stream(stream))
     _raise(rc, "gla_decode_step_paged")
+
+
+def gla_decode_step_gated(q, k, v, g, log_decay, state_inout, out, gate_kind: int = GATE_SILU, stream=None) -> None:
+    """bf16 decode step with the output gate fused into ``out`` (``g`` shaped like ``out``)."""
+    N, H, dk, dv = _decode_args(q, k, v, log_decay, state_inout, out, torch.bfloat16)
+    _check(g, "g", torch.bfloat16, (N, H, dv))
+    rc = load().gla_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), int(gate_kind), _ptr(log_decay),
+                                      _ptr(state_inout), _ptr(out), N, H, dk, dv, _stream(stream))
+    _raise(rc, "gla_decode_step_gated")
+
+
+def gla_decode_step_paged_gated(q, k, v, g, log_decay, state_pool, slots, out, gate_kind: int = GATE_SILU,
+                                stream=None) -> None:
+    """The paged decode step with the output gate fused into ``out``."""
+    if q.dim() != 3 or state_pool.dim() != 4:
+        raise ValueError("q must be [N, H, dk] and state_pool [nslots, H, dk, dv]")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (N, H, dk))
+    _check(v, "v", torch.bfloat16, (N, H, dv))
+    _check(g, "g", torch.bfloat16, (N, H, dv))
+    _check(out, "out", torch.bfloat16, (N, H, dv))
+    _check(log_decay, "log_decay", torch.float32, (H,))
+    _check(state_pool, "state_pool", torch.float32, (state_pool.shape[0], H, dk, dv))
+    _check(slots, "slots", torch.int32, (N,))
+    rc = load().gla_decode_step_paged_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), int(gate_kind), _ptr(log_decay),
+                                            _ptr(state_pool), _ptr(slots), int(state_pool.shape[0]), _ptr(out), N, H,
+                                            dk, dv, _stream(stream))
+    _raise(rc, "gla_decode_step_paged_gated")
 
 
 def _conv_args(x, weight, bias, state_in, state_out, y, cu_seqlens, dtype):

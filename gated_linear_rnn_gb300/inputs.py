@@ -153,6 +153,14 @@ def make_backward(w: Workload, device="cpu", seed: int = 0, lengths=None, T: Opt
     return d
 
 
+def make_gate(shape, device="cpu", seed: int = 0, scale: float = 2.0, dtype=torch.bfloat16):
+    """Output-gate pre-activations g shaped like the output (``shape``): N(0, scale^2), seeded.  A
+    spread of 2 puts the gate factors well into both of its tails."""
+    dev = torch.device(device)
+    g = _gen(dev, seed + 7919)
+    return _randn(tuple(shape), g, dev, scale).to(dtype)
+
+
 def make_decode(w: Workload, device="cpu", seed: int = 0, N: Optional[int] = None):
     """Inputs for one decode step: q, k [N,H,dk], v [N,H,dv] (``w.dtype``), state fp32."""
     dev = torch.device(device)

@@ -62,6 +62,14 @@ typedef enum {
     GLA_ERR_SCRATCH_LIMIT = -8 /* gla_chunk_fwd_noalloc: the problem needs more than its fixed scratch array */
 } gla_status;
 
+/* Output gate of the *_gated entry points (page "线性注意力模型如何实现固定推理状态", section
+ * "i14 与 Laplace 3B 架构", QKVG projection: the projection also yields a gate g_t of H x dv values per
+ * token, applied after the mixer; the page gives no formula, so both usual forms are offered). */
+typedef enum {
+    GLA_GATE_SILU = 0,    /* out = o * g / (1 + exp(-g))   (swish) */
+    GLA_GATE_SIGMOID = 1  /* out = o / (1 + exp(-g)) */
+} gla_gate_kind;
+
 /*
  * gla_chunk_fwd — chunkwise-parallel prefill / training forward, bf16 q, k, v, out.
  *
@@ -106,6 +114,21 @@ typedef enum {
 GLA_API int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_decay,
                   const float *h0, void *out, float *hT, int B, int T, int H, int dk, int dv,
                   int chunk, const int32_t *cu_seqlens, void *stream);
+
+/*
+ * gla_chunk_fwd_gated — gla_chunk_fwd with the output gate fused into the write of out:
+ *     out[t, h, :] = o_t,h * f(g[t, h, :])   elementwise, f per gate_kind (gla_gate_kind)
+ * where o is what gla_chunk_fwd computes; hT is unchanged by the gate.
+ *   g          [B, T, H, dv] bf16 (packed [1, T, H, dv]), the layout of out; device, 16-byte aligned;
+ *              read only (it may not alias out)
+ *   gate_kind  GLA_GATE_SILU or GLA_GATE_SIGMOID (else GLA_ERR_ARG)
+ *   all other arguments, the schedules and the errors: as gla_chunk_fwd.
+ * The gate costs one extra read of H * dv bf16 per token (1,536 instead of 1,152 bytes per token-head
+ * at dk 96, dv 192) and no extra launch.  Returns a gla_status.
+ */
+GLA_API int gla_chunk_fwd_gated(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                                const float *log_decay, const float *h0, void *out, float *hT, int B, int T,
+                                int H, int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream);
 
 /*
  * gla_chunk_fwd_noalloc — gla_chunk_fwd for callers that may not allocate device memory.
@@ -319,6 +342,22 @@ GLA_API int gla_decode_step_f32(const float *q, const float *k, const float *v, 
 GLA_API int gla_decode_step_paged(const void *q, const void *k, const void *v, const float *log_decay,
                                   float *state_pool, const int32_t *slots, int nslots, void *out, int N, int H,
                                   int dk, int dv, void *stream);
+
+/*
+ * gla_decode_step_gated / gla_decode_step_paged_gated — the decode steps with the output gate fused
+ * into the write of out: out[n, h, :] = (q S)[:] * f(g[n, h, :]), f per gate_kind (gla_gate_kind).  The
+ * state update is unchanged.  A padding row of the paged form still writes zeros.
+ *   g          [N, H, dv] bf16, the layout of out; device, 16-byte aligned; read only
+ *   gate_kind  GLA_GATE_SILU or GLA_GATE_SIGMOID (else GLA_ERR_ARG)
+ *   the other arguments and errors: as gla_decode_step / gla_decode_step_paged.
+ */
+GLA_API int gla_decode_step_gated(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                                  const float *log_decay, float *state_inout, void *out, int N, int H, int dk,
+                                  int dv, void *stream);
+GLA_API int gla_decode_step_paged_gated(const void *q, const void *k, const void *v, const void *g,
+                                        int gate_kind, const float *log_decay, float *state_pool,
+                                        const int32_t *slots, int nslots, void *out, int N, int H, int dk,
+                                        int dv, void *stream);
 
 /*
  * gla_conv1d_silu — causal depthwise Conv1d of width 4 followed by SiLU, per

@@ -348,6 +348,9 @@ def run_ours(args, world, rank, local):
     # ---- paged decode: the same step through a slot table (a permutation of the state pages) ----
     paged = run_paged_decode(args, D, wd, dout, stream, peaks)
 
+    # ---- the layer prefill with the output gate fused into its epilogue ----
+    gated = run_gated_prefill(args, P, w, out, hT, stream, peaks)
+
     # ---- causal conv1d + SiLU over the layer's residual stream, and its per-token step ----
     conv = run_conv(args, w, wd, stream, peaks, dev)
 
@@ -377,6 +380,7 @@ def run_ours(args, world, rank, local):
                    "tokens_per_s": wd.B * world / dec_avg_s},
         "e2e": e2e,
         "decode_paged": paged,
+        "prefill_gated": gated,
         "conv1d_silu": conv,
         "backward": bwd,
         "train_step": train,
@@ -422,6 +426,38 @@ def run_paged_decode(args, D, wd, dout, stream, peaks):
     return {"us_per_step": us, "unit": "state GB/s", "value": sbytes / (us / 1e6) / 1e9,
             "frac_of_hbm_peak": (sbytes + iobytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"], "steps": n,
             "rows": wd.B, "pool_pages": wd.B}
+
+
+def run_gated_prefill(args, P, w, out, hT, stream, peaks):
+    """gla_chunk_fwd_gated on the layer workload (SiLU gate, g seeded like the output): the output gate
+    fused into the forward's epilogue; CUDA events per launch, median.  Algorithmic bytes add one bf16
+    read of g per output element to the plain forward's."""
+    import torch
+    from gated_linear_rnn_gb300 import gla, inputs as I
+    g = I.make_gate(out.shape, device=out.device, seed=5)
+    C = w.chunk
+
+    def step():
+        gla.gla_chunk_fwd_gated(P["q"], P["k"], P["v"], g, P["log_decay"], P["h0"], out, hT, C, None,
+                                gate_kind=gla.GATE_SILU, stream=stream)
+
+    for _ in range(3):
+        step()
+    n = max(3, min(args.steps, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for e in ev:
+        e[0].record(stream)
+        step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the gated prefill: {st_code} ({gla.gla_status_str(st_code)})")
+    us = statistics.median(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    nbytes = prefill_bytes(w.B, w.T, w.H, w.dk, w.dv, P["h0"] is not None, True) + w.B * w.T * w.H * w.dv * 2
+    return {"us": us, "unit": "tokens/s", "value": w.B * w.T / (us / 1e6), "algorithmic_bytes": nbytes,
+            "achieved_gbs": nbytes / (us / 1e6) / 1e9, "frac_of_hbm_peak": nbytes / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
+            "steps": n, "gate": "silu", "kernel": "gla_chunk_fwd_gated (layer_bf16)"}
 
 
 def run_conv(args, w, wd, stream, peaks, dev, D=3072):

@@ -351,6 +351,9 @@ def run_ours(args, world, rank, local):
     # ---- the layer prefill with the output gate fused into its epilogue ----
     gated = run_gated_prefill(args, P, w, out, hT, stream, peaks)
 
+    # ---- decode over pages holding all 24 layers of a sequence ----
+    layers = run_decode_layers(args, wd, stream, peaks, dev)
+
     # ---- causal conv1d + SiLU over the layer's residual stream, and its per-token step ----
     conv = run_conv(args, w, wd, stream, peaks, dev)
 
@@ -381,6 +384,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "decode_paged": paged,
         "prefill_gated": gated,
+        "decode_layers": layers,
         "conv1d_silu": conv,
         "backward": bwd,
         "train_step": train,
@@ -458,6 +462,51 @@ def run_gated_prefill(args, P, w, out, hT, stream, peaks):
     return {"us": us, "unit": "tokens/s", "value": w.B * w.T / (us / 1e6), "algorithmic_bytes": nbytes,
             "achieved_gbs": nbytes / (us / 1e6) / 1e9, "frac_of_hbm_peak": nbytes / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
             "steps": n, "gate": "silu", "kernel": "gla_chunk_fwd_gated (layer_bf16)"}
+
+
+def run_decode_layers(args, wd, stream, peaks, dev, N=128, L=24):
+    """gla_decode_step_layers: N sequences whose pages hold all L layers (the 24-layer model), one
+    launch for every layer, and the same step as L one-layer launches; CUDA events, median."""
+    import torch
+    from gated_linear_rnn_gb300 import gla, inputs as I
+    H, dk, dv = wd.H, wd.dk, wd.dv
+    g = torch.Generator(device=dev).manual_seed(13)
+    q = (torch.randn(L, N, H, dk, generator=g, device=dev) / dk ** 0.5).to(torch.bfloat16)
+    k = (torch.randn(L, N, H, dk, generator=g, device=dev) / dk ** 0.5).to(torch.bfloat16)
+    v = torch.randn(L, N, H, dv, generator=g, device=dev).to(torch.bfloat16)
+    ld = torch.stack([I.log_decays(H, wd.decay_lo, wd.decay_hi)] * L).to(dev)
+    pool = torch.randn(N, L, H, dk, dv, generator=g, device=dev).mul_(0.02)
+    slots = torch.randperm(N, device="cpu", generator=torch.Generator().manual_seed(13)).to(torch.int32).to(dev)
+    out = torch.empty(L, N, H, dv, dtype=torch.bfloat16, device=dev)
+
+    def one():
+        gla.gla_decode_step_layers(q, k, v, ld, pool, slots, out, stream=stream)
+
+    def per_layer():
+        for l in range(L):
+            gla.gla_decode_step_layers(q[l:l + 1], k[l:l + 1], v[l:l + 1], ld[l:l + 1], pool, slots, out[l:l + 1],
+                                       layer0=l, stream=stream)
+
+    res = {}
+    for name, fn in (("one_launch", one), ("per_layer", per_layer)):
+        for _ in range(3):
+            fn()
+        n = max(3, min(args.steps, 30))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for e in ev:
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.median(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the multi-layer decode: {st_code} ({gla.gla_status_str(st_code)})")
+    sbytes, iobytes = decode_bytes(N * L, H, dk, dv)
+    us = res["one_launch"]
+    return {"us_one_launch": us, "us_per_layer_launches": res["per_layer"], "unit": "state GB/s",
+            "value": sbytes / (us / 1e6) / 1e9, "frac_of_hbm_peak": (sbytes + iobytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
+            "sequences": N, "layers": L, "pool_bytes": pool.numel() * 4}
 
 
 def run_conv(args, w, wd, stream, peaks, dev, D=3072):

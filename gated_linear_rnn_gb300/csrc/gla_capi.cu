@@ -55,6 +55,8 @@ int simt_chunk_fwd_gated_bf16(const void *, const void *, const void *, const vo
                               cudaStream_t);
 int decode_step_gated_bf16(const void *, const void *, const void *, const void *, int, const float *, float *,
                            const int32_t *, int, void *, int, int, int, int, cudaStream_t);
+int decode_step_layers_bf16(const void *, const void *, const void *, const void *, int, const float *, float *,
+                            const int32_t *, int, int, int, int, void *, int, int, int, int, cudaStream_t);
 int take_status_conv(cudaStream_t);
 int take_status_simt(cudaStream_t);
 int take_status_bwd(cudaStream_t);
@@ -312,6 +314,22 @@ int gla_decode_step_paged_gated(const void *q, const void *k, const void *v, con
     if ((long long)nslots * H > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     return decode_step_gated_bf16(q, k, v, g, gate_kind, log_decay, state_pool, slots, nslots, out, N, H, dk, dv,
                                   (cudaStream_t)stream);
+}
+
+int gla_decode_step_layers(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                           const float *log_decay, float *state_pool, const int32_t *slots, int nslots,
+                           int page_layers, int layer0, int L, void *out, int N, int H, int dk, int dv,
+                           void *stream) {
+    if (!slots || nslots <= 0 || L <= 0 || page_layers <= 0 || layer0 < 0 || layer0 > page_layers - L)
+        return GLA_ERR_ARG;
+    if (g && gate_kind != GLA_GATE_SILU && gate_kind != GLA_GATE_SIGMOID) return GLA_ERR_ARG;
+    if (N <= 0 || (long long)L * N > 0x7fffffffLL) return GLA_ERR_ARG;
+    int rc = check_decode(q, k, v, log_decay, state_pool, out, L * N, H, dk, dv);
+    if (rc) return rc;
+    if (!aligned16(g) || !aligned16(slots)) return GLA_ERR_ALIGN;
+    if ((long long)L * N * H > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
+    return decode_step_layers_bf16(q, k, v, g, gate_kind, log_decay, state_pool, slots, nslots, page_layers, layer0,
+                                   L, out, N, H, dk, dv, (cudaStream_t)stream);
 }
 
 int gla_conv1d_silu(const void *x, const float *weight, const float *bias, const float *state_in, float *state_out,

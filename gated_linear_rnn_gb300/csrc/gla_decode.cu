@@ -55,23 +55,25 @@ __global__ void __launch_bounds__(kMaxThreads)
 decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
               const float *__restrict__ log_decay, float *__restrict__ state, T *__restrict__ out,
               int H, int dk, int dv, const int32_t *__restrict__ slots, int nslots, const T *__restrict__ gate,
-              int gate_kind) {
+              int gate_kind, int rows, int page_layers, int layer0) {
     extern __shared__ float sm[];
     float *qs = sm, *ks = sm + dk, *red = sm + 2 * dk;  // red: [kRG][dv]
-    const int unit = blockIdx.x;                          // n * H + h
+    // unit = (l * rows + n) * H + h: layer l of the call, batch row n, head h (one layer: l = 0)
+    const int unit = blockIdx.x;
     const int h = unit % H;
+    const int n = (unit / H) % rows, l = unit / (H * rows);
     const int ncg = dv >> 2;
     const int tid = threadIdx.x;
     const int cg = tid % ncg, rg = tid / ncg;
     // the slot (paged form) and q, k, v are independent loads: all in flight at once
-    const int slot = slots != nullptr ? __ldg(slots + unit / H) : 0;
+    const int slot = slots != nullptr ? __ldg(slots + n) : 0;
     for (int i = tid; i < dk; i += blockDim.x) {
         qs[i] = to_f32(q[(size_t)unit * dk + i]);
         ks[i] = to_f32(k[(size_t)unit * dk + i]);
     }
     float vv[4];
     load4<T>(v + (size_t)unit * dv + cg * 4, vv);
-    const float lam = expf(__ldg(log_decay + h));
+    const float lam = expf(__ldg(log_decay + (size_t)l * H + h));
     size_t page = (size_t)unit;  // state page of this (n, h): unit itself unless paged
     if (slots != nullptr) {
         if (slot < 0 || slot >= nslots) {  // padding row (or a bad slot, reported): zero output, no page
@@ -79,7 +81,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
             for (int c = tid; c < dv; c += blockDim.x) out[(size_t)unit * dv + c] = from_f32<T>(0.f);
             return;
         }
-        page = (size_t)slot * H + h;
+        page = ((size_t)slot * page_layers + layer0 + l) * H + h;  // layer layer0 + l of page `slot`
     }
 
     float4 *S = reinterpret_cast<float4 *>(state + page * dk * dv) + cg;
@@ -133,18 +135,20 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 template <typename T>
 int launch_decode(const T *q, const T *k, const T *v, const float *ld, float *state, T *out, int N, int H,
                   int dk, int dv, cudaStream_t st, const int32_t *slots = nullptr, int nslots = 0,
-                  const T *gate = nullptr, int gate_kind = 0) {
-    const long long units = (long long)N * H;
+                  const T *gate = nullptr, int gate_kind = 0, int L = 1, int page_layers = 1, int layer0 = 0) {
+    const long long units = (long long)L * N * H;
     if (units > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     const int threads = (dv / 4) * kRG;
     if (threads > 1024) return GLA_ERR_UNSUPPORTED;
     const size_t bytes = (size_t)(2 * dk + kRG * dv) * sizeof(float);
     if (threads <= 256)
         decode_kernel<T, 256, 12><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv,
-                                                                           slots, nslots, gate, gate_kind);
+                                                                           slots, nslots, gate, gate_kind, N,
+                                                                           page_layers, layer0);
     else
         decode_kernel<T, 1024, 4><<<(unsigned)units, threads, bytes, st>>>(q, k, v, ld, state, out, H, dk, dv,
-                                                                           slots, nslots, gate, gate_kind);
+                                                                           slots, nslots, gate, gate_kind, N,
+                                                                           page_layers, layer0);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
@@ -168,6 +172,17 @@ int decode_step_paged_bf16(const void *q, const void *k, const void *v, const fl
     using B = __nv_bfloat16;
     return launch_decode<B>((const B *)q, (const B *)k, (const B *)v, ld, pool, (B *)out, N, H, dk, dv, st, slots,
                             nslots);
+}
+
+// L layers of a step in one launch: q, k [L, N, H, dk], v, out (and gate) [L, N, H, dv], log_decay
+// [L, H]; layer l of row n uses layer layer0 + l of page slots[n] in a pool of pages of page_layers
+// layers ([nslots, page_layers, H, dk, dv]).
+int decode_step_layers_bf16(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                            const float *ld, float *pool, const int32_t *slots, int nslots, int page_layers,
+                            int layer0, int L, void *out, int N, int H, int dk, int dv, cudaStream_t st) {
+    using B = __nv_bfloat16;
+    return launch_decode<B>((const B *)q, (const B *)k, (const B *)v, ld, pool, (B *)out, N, H, dk, dv, st, slots,
+                            nslots, (const B *)g, gate_kind, L, page_layers, layer0);
 }
 
 // The step with the output gate applied to o (slots null: the dense state layout).

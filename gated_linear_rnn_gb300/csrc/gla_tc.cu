@@ -112,7 +112,7 @@ constexpr int kLptMaxSeq = 256;
 
 // Shared memory plan (bytes from the 1024-aligned base).
 struct Smem {
-    uint32_t q, q1, k0, k1, v0, v1, s, xp, tab, utab, bars, slot, abort, total;
+    uint32_t q, q1, k0, k1, v0, v1, s, gb, xp, tab, utab, bars, slot, abort, total;
 };
 
 // Barriers, lookup tables and the TMEM slot after the tiles at offset `at`.
@@ -138,6 +138,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
     p.v0 = p.k1 + qk;  // MMA4 reads up to 4 atoms from a K tile: V follows, so the over-read stays in bounds
     p.v1 = p.v0 + vv;
     p.s = p.v1 + vv;
+    p.gb = 0;
     smem_plan_tail(p, p.s + (uint32_t)dk * 128u * (uint32_t)(dv / 64));
     return p;
 }
@@ -146,7 +147,7 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 // current one is still read, and no state-copy tile of its own.  The bf16 copy of S_{c-1} that MMA3(c)
 // reads is written into the V tile of chunk c-1 (free once MMA2(c-1) and MMA4(c-1) are done; dk <= 128
 // rows of dv bf16 fit in its 128 rows), and V(c+1) lands there once MMA3(c) has read it.
-__host__ __device__ inline Smem smem_plan_full(int dk, int dv) {
+__host__ __device__ inline Smem smem_plan_full(int dk, int dv, bool gate = false) {
     Smem p;
     const uint32_t qk = (uint32_t)(dk / 32) * 8192u;
     const uint32_t vv = (uint32_t)(dv / 64) * 16384u;
@@ -157,7 +158,8 @@ __host__ __device__ inline Smem smem_plan_full(int dk, int dv) {
     p.v0 = p.k1 + qk;  // as above: the over-read of K1 by MMA4 stays inside V0
     p.v1 = p.v0 + vv;
     p.s = p.v0;        // no tile of its own (see above)
-    smem_plan_tail(p, p.v1 + vv);
+    p.gb = p.v1 + vv;  // gated instance: 4 x 4 KB of output-gate rows (one 64-column group per epilogue warp)
+    smem_plan_tail(p, p.gb + (gate ? 4u * 4096u : 0u));
     return p;
 }
 
@@ -175,6 +177,22 @@ __device__ __forceinline__ int b_kvfull(int s) { return s == 0 ? B_KVFULL0 : s =
 __device__ __forceinline__ int b_kvempty(int s) { return s == 0 ? B_KVEMPTY0 : s == 1 ? B_KVEMPTY1 : B_KVEMPTY2; }
 __device__ __forceinline__ int b_kprep(int s) { return s == 0 ? B_KPREP0 : s == 1 ? B_KPREP1 : B_KPREP2; }
 static_assert(B_COUNT <= 32, "the shared-memory plan reserves 32 barrier slots");
+
+// Output-gate factors in the tensor-core epilogue, which drains O on the chunk loop's critical path: two
+// gate values at a time in bf16 pairs, sigmoid(g) = (1 + tanh(g/2)) / 2 and SiLU(g) = g sigmoid(g) with the
+// hardware tanh approximation (one MUFU operation per pair).  The factors carry bf16 precision and an
+// absolute sigmoid error of a few 1e-3 at most, about the bf16 rounding of the output itself.
+__device__ __forceinline__ uint32_t gate_factor_bf16x2(uint32_t g2, int kind) {
+    const uint32_t half2 = 0x3f003f00u;  // (0.5, 0.5) in bf16
+    uint32_t hg, t, f;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hg) : "r"(g2), "r"(half2));
+    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(hg));
+    if (kind == 0)
+        asm("fma.rn.bf16x2 %0, %1, %2, %1;" : "=r"(f) : "r"(hg), "r"(t));  // hg t + hg
+    else
+        asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(f) : "r"(t), "r"(half2));  // t / 2 + 1 / 2
+    return f;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -222,9 +240,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int dk = P.dk, dv = P.dv, H = P.H;
     const int nka = dk / 32, nva = dv / 64;
     // shared-memory offsets (scalars: nothing of the plan lives in local memory)
-    const Smem plan = kFull ? smem_plan_full(dk, dv) : smem_plan(dk, dv);
+    const Smem plan = kFull ? smem_plan_full(dk, dv, kGate) : smem_plan(dk, dv);
     const uint32_t o_q = plan.q, o_k0 = plan.k0, o_k1 = plan.k1, o_v0 = plan.v0, o_v1 = plan.v1, o_s = plan.s;
-    const uint32_t o_q1 = plan.q1;
+    const uint32_t o_q1 = plan.q1, o_gb = plan.gb;
     const uint32_t o_xp = plan.xp;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + plan.bars;
@@ -961,7 +979,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         bool ok = true;
         // O is free for the first chunk's MMA3 (the releases of O count toward SREADY, one phase later)
         if (!state_only && nchunks > 0 && lane == 0) mbar_arrive(BAR(B_SREADY));
-        for (int c = 0; c < nchunks && ok && !state_only; ++c) {
+        for (int c = 0; c < nchunks && ok && !state_only && !kGate; ++c) {
             const int Lc = chunk_len(c);
             // ---- output epilogue: O -> bf16 rows in this warp's 4 KB staging tile (one 64-column
             // group of its 32 rows, laid out as a 128B-swizzled TMA box), then a TMA store per group.
@@ -973,13 +991,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const bool full = (Lc == kC);
             for (int j0 = 0; j0 < dv; j0 += 64) {
                 uint32_t v[2][32];
-                // output gate of this row's 64 columns (8 x 8 bf16), in flight with the TMEM loads
-                uint4 gv[kGate ? 8 : 1];
-                if (kGate) {
-                    const uint4 *gp = reinterpret_cast<const uint4 *>(P.gate + ((row0 + (int64_t)c * kC + r) * H + h) * dv + j0);
-#pragma unroll
-                    for (int i = 0; i < (kGate ? 8 : 1); ++i) gv[i] = (r < Lc) ? __ldg(gp + i) : make_uint4(0u, 0u, 0u, 0u);
-                }
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0 + 32u, v[1]);
                 tmem_wait_ld();
@@ -994,17 +1005,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 uint8_t *myrow = xp + (uint32_t)lane * 128u;
 #pragma unroll
                 for (int q8 = 0; q8 < 8; ++q8) {
-                    uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
-                    if (kGate) {
-                        const uint32_t gw[4] = {gv[kGate ? q8 : 0].x, gv[kGate ? q8 : 0].y, gv[kGate ? q8 : 0].z,
-                                                gv[kGate ? q8 : 0].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[e]));
-                            x[2 * e] = __float_as_uint(__uint_as_float(x[2 * e]) * gate_factor(gf.x, P.gate_kind));
-                            x[2 * e + 1] = __float_as_uint(__uint_as_float(x[2 * e + 1]) * gate_factor(gf.y, P.gate_kind));
-                        }
-                    }
+                    const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
                     *reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4)) = make_uint4(
                         pack_bf16x2(__uint_as_float(x[0]) * grow, __uint_as_float(x[1]) * grow),
                         pack_bf16x2(__uint_as_float(x[2]) * grow, __uint_as_float(x[3]) * grow),
@@ -1030,6 +1031,112 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         if (row < Lc) {
                             const uint4 x = *reinterpret_cast<const uint4 *>(
                                 xp + (uint32_t)rr * 128u + (((uint32_t)ch ^ (uint32_t)(rr & 7)) << 4));
+                            *reinterpret_cast<uint4 *>(P.out + ((row0 + (int64_t)c * kC + row) * H + h) * dv + j0 +
+                                                       8 * ch) = x;
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        // ---- gated instance: out = O * f(g).  The gate rows of a 64-column group (the warp's 32 rows x
+        // 128 bytes) are copied four rows per instruction (coalesced cp.async, no registers) into one of
+        // two 4 KB buffers, the gate buffer and the staging tile, alternating by group and laid out as the
+        // staging tile; each lane turns its own row of gate values into its row of gated output in place,
+        // and the group's TMA store goes out of that buffer.  The first two groups' gates are copied before
+        // O is ready, each later one as soon as the store two groups back has read its buffer; the next
+        // chunk's gate lines are prefetched into L2. ----
+        for (int c = 0; c < nchunks && ok && kGate; ++c) {
+            const int Lc = chunk_len(c);
+            const int ng = dv / 64, gk = P.gate_kind;
+            auto buf_of = [&](int j) -> uint32_t { return ((j & 1) ? o_xp : o_gb) + (uint32_t)q4 * 4096u; };
+            auto copy_gate = [&](int j) {
+                const uint32_t dst = sbase + buf_of(j);
+                const int rr0 = 32 * q4 + (lane >> 3);
+                const uint4 *gp = reinterpret_cast<const uint4 *>(
+                                      P.gate + ((row0 + (int64_t)c * kC + rr0) * H + h) * dv + 64 * j) + (lane & 7);
+                const int64_t step = (int64_t)H * dv / 2;  // four rows, in 16-byte units
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t row = 4u * (uint32_t)i + (uint32_t)(lane >> 3);
+                    const bool valid = rr0 + 4 * i < Lc;
+                    cp_async16(dst + row * 128u + ((((uint32_t)lane & 7u) ^ (row & 7u)) << 4),
+                               valid ? (const void *)(gp + i * step) : (const void *)P.gate, valid);
+                }
+                cp_async_commit();
+            };
+            if (c + 1 < nchunks && r < chunk_len(c + 1)) {
+                const __nv_bfloat16 *gn = P.gate + ((row0 + (int64_t)(c + 1) * kC + r) * H + h) * dv;
+                for (int j0 = 0; j0 < dv; j0 += 64)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(gn + j0)));
+            }
+            if (lane == 0) bulk_wait_read0();  // both buffers: the previous chunk's stores have read them
+            __syncwarp();
+            copy_gate(0);
+            if (ng > 1) copy_gate(1);
+            ok = mbar_wait(BAR(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
+            if (!ok) break;
+            tc_fence_after();
+            const bool full = (Lc == kC);
+            for (int j = 0; j < ng; ++j) {
+                const int j0 = 64 * j;
+                uint32_t v[2][32];
+                tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
+                tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0 + 32u, v[1]);
+                // gate j has landed (in the first group the copy of gate 1 may still be in flight)
+                if (j == 0 && ng > 1)
+                    cp_async_wait_1();
+                else
+                    cp_async_wait_all();
+                __syncwarp();  // every lane's copies
+                // the gate of group j + 1 goes where group j - 1 was staged, once that store has read it
+                if (j >= 1 && j + 1 < ng) {
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                    copy_gate(j + 1);
+                }
+                tmem_wait_ld();
+                if (j + 1 == ng) {  // last TMEM read of O for this chunk: MMA3 of the next chunk may start
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(B_SREADY));
+                }
+                // own row (lane): 64 gate values -> 64 gated outputs in place, 16-byte chunk q8 at q8 ^ (lane & 7)
+                uint8_t *myrow = smem + buf_of(j) + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    uint4 *cell = reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4));
+                    const uint4 gq = *cell;
+                    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                    const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
+                    uint32_t o2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t f2 = gate_factor_bf16x2(gw[e], gk);
+                        const float2 ff = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&f2));
+                        o2[e] = pack_bf16x2(__uint_as_float(x[2 * e]) * grow * ff.x,
+                                            __uint_as_float(x[2 * e + 1]) * grow * ff.y);
+                    }
+                    *cell = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                }
+                if (full) {
+                    fence_async_shared();  // the staged rows must be visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmO, h * dv + j0, row0 + c * kC + 32 * q4, sbase + buf_of(j));
+                        bulk_commit();
+                    }
+                } else {
+                    // partial chunk: plain predicated stores of the rows below Lc (as in the plain epilogue)
+                    __syncwarp();
+                    const int ch = lane & 7;
+                    const uint8_t *tile = smem + buf_of(j);
+#pragma unroll 4
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3), row = 32 * q4 + rr;
+                        if (row < Lc) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(
+                                tile + (uint32_t)rr * 128u + (((uint32_t)ch ^ (uint32_t)(rr & 7)) << 4));
                             *reinterpret_cast<uint4 *>(P.out + ((row0 + (int64_t)c * kC + row) * H + h) * dv + j0 +
                                                        8 * ch) = x;
                         }
@@ -1147,6 +1254,12 @@ bool tc_chunk_supported(int dk, int dv, int chunk) {
     return smem_plan(dk, dv).total + 1024 <= cap && smem_plan_full(dk, dv).total + 1024 <= cap;
 }
 
+// The gated full pass also needs its 16 KB of gate rows.
+bool tc_gate_supported(int dk, int dv) {
+    return tc_chunk_supported(dk, dv, kC) &&
+           smem_plan_full(dk, dv, true).total + 1024 <= (uint32_t)device_info().max_smem_optin;
+}
+
 namespace {
 
 // Segments per chain for a dense batch: as many as fill one wave of CTAs (one per SM), each at
@@ -1177,7 +1290,7 @@ bool three_stages_fit(int dk, int dv) {
 template <bool kRev, int kNst, bool kFull, bool kGate = false>
 int launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                const Params &p, long long ctas, cudaStream_t st) {
-    const size_t bytes = (kFull ? smem_plan_full(p.dk, p.dv) : smem_plan(p.dk, p.dv)).total + 1024;  // + alignment slack
+    const size_t bytes = (kFull ? smem_plan_full(p.dk, p.dv, kGate) : smem_plan(p.dk, p.dv)).total + 1024;  // + alignment slack
     if (cudaFuncSetAttribute(gla_tc_chunk_kernel<kRev, kNst, kFull, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bytes) != cudaSuccess)
         return GLA_ERR_LAUNCH;

@@ -30,6 +30,7 @@ SIGNATURES = {
     "gla_chunk_fwd_gated": ([_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_decode_step_gated": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "gla_decode_step_paged_gated": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P], _I),
+    "gla_decode_step_layers": ([_P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _P], _I),
     "gla_chunk_fwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "gla_chunk_fwd_host": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "gla_chunk_fwd_f32": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
@@ -356,6 +357,30 @@ def gla_decode_step_paged_gated(q, k, v, g, log_decay, state_pool, slots, out, g
                                             _ptr(state_pool), _ptr(slots), int(state_pool.shape[0]), _ptr(out), N, H,
                                             dk, dv, _stream(stream))
     _raise(rc, "gla_decode_step_paged_gated")
+
+
+def gla_decode_step_layers(q, k, v, log_decay, state_pool, slots, out, layer0: int = 0, g=None,
+                           gate_kind: int = GATE_SILU, stream=None) -> None:
+    """Decode steps of L layers in one launch over pages of ``page_layers`` layers: q, k [L, N, H, dk],
+    v, out (and g) [L, N, H, dv], log_decay [L, H], state_pool [nslots, page_layers, H, dk, dv], slots [N].
+    Layer l of the call uses layer ``layer0 + l`` of page slots[n]."""
+    if q.dim() != 4 or state_pool.dim() != 5:
+        raise ValueError("q must be [L, N, H, dk] and state_pool [nslots, page_layers, H, dk, dv]")
+    L, N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (L, N, H, dk))
+    _check(v, "v", torch.bfloat16, (L, N, H, dv))
+    _check(out, "out", torch.bfloat16, (L, N, H, dv))
+    _check(g, "g", torch.bfloat16, (L, N, H, dv), allow_none=True)
+    _check(log_decay, "log_decay", torch.float32, (L, H))
+    nslots, page_layers = int(state_pool.shape[0]), int(state_pool.shape[1])
+    _check(state_pool, "state_pool", torch.float32, (nslots, page_layers, H, dk, dv))
+    _check(slots, "slots", torch.int32, (N,))
+    rc = load().gla_decode_step_layers(_ptr(q), _ptr(k), _ptr(v), _ptr(g), int(gate_kind), _ptr(log_decay),
+                                       _ptr(state_pool), _ptr(slots), nslots, page_layers, int(layer0), L, _ptr(out),
+                                       N, H, dk, dv, _stream(stream))
+    _raise(rc, "gla_decode_step_layers")
 
 
 def _conv_args(x, weight, bias, state_in, state_out, y, cu_seqlens, dtype):

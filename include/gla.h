@@ -351,6 +351,29 @@ GLA_API int gla_decode_step_paged(const void *q, const void *k, const void *v, c
  *   gate_kind  GLA_GATE_SILU or GLA_GATE_SIGMOID (else GLA_ERR_ARG)
  *   the other arguments and errors: as gla_decode_step / gla_decode_step_paged.
  */
+/*
+ * gla_decode_step_layers — decode steps of L layers at once over pages that hold every layer of a
+ * sequence (page "线性注意力模型如何实现固定推理状态", section "Trainium2 上的推理优化": the serving
+ * engine gives each sequence one fixed state page for the whole model, and every new batch width cost
+ * a separately compiled shape).  Pages are [page_layers, H, dk, dv] f32; row n of the batch uses page
+ * slots[n], and layer l (0 <= l < L) of the call updates and reads layer layer0 + l of it:
+ *     S = state_pool[slots[n], layer0 + l, h]:  S <- lambda_{l,h} S + k^T v;  out[l, n, h] = q S
+ * (times the output gate's factor when g is given).  One launch covers L * N * H chains with the same
+ * kernel for any L and N.  A model whose layer l + 1 needs layer l's output calls it once per layer
+ * (L = 1, layer0 = l); L > 1 serves inputs of several layers that are ready together.
+ *   q, k         [L, N, H, dk] bf16;  v, out [L, N, H, dv] bf16
+ *   g            [L, N, H, dv] bf16 or NULL (no gate);  gate_kind as gla_chunk_fwd_gated when g is given
+ *   log_decay    [L, H] f32: the decays of layers layer0 .. layer0 + L - 1
+ *   state_pool   [nslots, page_layers, H, dk, dv] f32, read and written in place
+ *   slots        [N] int32 on the device; negative: a padding row (zero out, no page touched)
+ *   0 <= layer0, layer0 + L <= page_layers (else GLA_ERR_ARG); pointers 16-byte aligned; as
+ *   gla_decode_step_paged otherwise (two rows must not name the same page).
+ */
+GLA_API int gla_decode_step_layers(const void *q, const void *k, const void *v, const void *g, int gate_kind,
+                                   const float *log_decay, float *state_pool, const int32_t *slots, int nslots,
+                                   int page_layers, int layer0, int L, void *out, int N, int H, int dk, int dv,
+                                   void *stream);
+
 GLA_API int gla_decode_step_gated(const void *q, const void *k, const void *v, const void *g, int gate_kind,
                                   const float *log_decay, float *state_inout, void *out, int N, int H, int dk,
                                   int dv, void *stream);

@@ -74,3 +74,26 @@ def test_fuzz_forward_and_backward(case):
     for name, g, r in zip(("dq", "dk", "dv", "dh0"), grads, g_ref):
         errs[name] = oracle.rel_err(g.float().cpu().numpy(), r)
     assert all(e <= tol for e in errs.values()), (case, w.dtype, w.dk, w.dv, w.H, w.chunk, kw, errs)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_fuzz_gated_forward(case):
+    """The forward with the output gate (bf16 only) over the same seeded draws, both gate forms."""
+    w, kw, _ = draw(case)
+    w = I.scaled(w, dtype="bf16")
+    kind = case % 2
+    d = I.make_prefill(w, device="cuda", seed=case, **kw)
+    cu = d["cu_seqlens"]
+    cu_dev = None if cu is None else cu.cuda()
+    nseq = d["q"].shape[0] if cu is None else cu.numel() - 1
+    out = torch.empty(d["q"].shape[:3] + (w.dv,), dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty(nseq, w.H, w.dk, w.dv, device="cuda")
+    g = I.make_gate(out.shape, device="cuda", seed=case)
+    gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], g, d["log_decay"], d["h0"], out, hT, w.chunk, cu_dev,
+                            gate_kind=kind)
+    torch.cuda.synchronize()
+    assert gla.gla_last_device_status() == 0
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], cu_seqlens=cu)
+    eo = oracle.rel_err(out.float().cpu().numpy(), oracle.output_gate(o_ref, g, kind))
+    eh = oracle.rel_err(hT.cpu().numpy(), h_ref)
+    assert eo <= 1e-2 and eh <= 1e-2, (case, kind, w.dk, w.dv, w.H, w.chunk, kw, eo, eh)

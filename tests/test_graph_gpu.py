@@ -133,3 +133,68 @@ def test_saved_states_training_step_in_a_graph():
         torch.cuda.synchronize()
         for name, g, r in zip(("out", "hT", "dq", "dk", "dv", "dh0"), (out, hT, dq, dk, dv, dh0), ref):
             assert torch.equal(g, r), f"{name} differs after replay (seed {seed})"
+
+
+@pytest.mark.parametrize("T", [640, 4096])  # whole chains; segmented (one long sequence per head)
+def test_gated_forward_and_layer_decode_in_a_graph(T):
+    """The gated forward and a multi-layer decode step captured in one graph replay bit-identically to
+    eager calls, also after new inputs are copied into the captured buffers."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=1 if T == 4096 else 2, T=T, H=4, h0_std=0.02)
+    L, N, nslots = 3, 8, 16
+
+    def inputs(seed):
+        d = I.make_prefill(w, device="cuda", seed=seed)
+        gen = torch.Generator().manual_seed(seed)
+        dec = {"q": (torch.randn(L, N, 4, 96, generator=gen) / 96 ** 0.5).to(torch.bfloat16).cuda(),
+               "k": (torch.randn(L, N, 4, 96, generator=gen) / 96 ** 0.5).to(torch.bfloat16).cuda(),
+               "v": torch.randn(L, N, 4, 192, generator=gen).to(torch.bfloat16).cuda(),
+               "pool": (torch.randn(nslots, L, 4, 96, 192, generator=gen) * 0.02).cuda(),
+               "slots": torch.randperm(nslots, generator=gen)[:N].to(torch.int32).cuda()}
+        g = I.make_gate(d["q"].shape[:3] + (192,), device="cuda", seed=seed)
+        return d, dec, g
+
+    ld_dec = torch.stack([I.log_decays(4)] * L).cuda()
+    d, dec, g = inputs(41)
+    out = torch.empty(d["q"].shape[:3] + (192,), dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty(d["q"].shape[0], 4, 96, 192, device="cuda")
+    dout = torch.empty(L, N, 4, 192, dtype=torch.bfloat16, device="cuda")
+    pool = dec["pool"].clone()
+
+    def step(s=None):
+        gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], g, d["log_decay"], d["h0"], out, hT, 128, stream=s)
+        gla.gla_decode_step_layers(dec["q"], dec["k"], dec["v"], ld_dec, pool, dec["slots"], dout, stream=s)
+
+    def eager_results():
+        pool.copy_(dec["pool"])
+        step()
+        torch.cuda.synchronize()
+        return out.clone(), hT.clone(), dout.clone(), pool.clone()
+
+    want = eager_results()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    pool.copy_(dec["pool"])
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=s):
+        step(s)
+    for round_ in range(2):
+        if round_ == 1:  # new inputs into the captured buffers
+            d2, dec2, g2 = inputs(42)
+            for key in ("q", "k", "v"):
+                d[key].copy_(d2[key])
+                dec[key].copy_(dec2[key])
+            g.copy_(g2)
+            dec["pool"].copy_(dec2["pool"])
+            dec["slots"].copy_(dec2["slots"])
+            if d["h0"] is not None:
+                d["h0"].copy_(d2["h0"])
+            want = eager_results()
+        pool.copy_(dec["pool"])
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        got = (out, hT, dout, pool)
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+    assert gla.gla_last_device_status() == 0

@@ -11,7 +11,9 @@
 //
 // One CTA owns one (sequence, head) chain and walks its 128-token chunks in
 // order with the f32 state resident in TMEM for the whole chain.  Per chunk the
-// four contractions are tcgen05.mma instructions (M = 128, K-steps of 16):
+// four contractions are tcgen05.mma instructions (M = 128, K-steps of 16), issued
+// in the order MMA1, MMA3, MMA2, MMA4 by the passes that write outputs (the
+// state-only passes run MMA4 alone):
 //   MMA1  A    = Q K^T                      TMEM cols [384, 512)   A: Q (smem), B: K (smem)
 //   MMA3  O    = (diag(lambda^(i+1)) Q) S   TMEM cols [0, dv)      A: Q' (smem), B: S bf16 (smem)
 //   MMA4  S   += (diag(lambda^(L-1-j)) K)^T V  TMEM cols [192, 192+dv)  A: K'^T (smem), B: V (smem)
@@ -33,10 +35,15 @@
 //              per tile; a tile is refilled once its previous store has read
 //              it.  O leaves TMEM at the pace of the TMEM loads, so MMA3 of
 //              the next chunk is not held up by global stores.  The mask of
-//              chunk c+1 and the epilogue of chunk c overlap.
-//   warp 8     TMA producer: Q (single buffer), K and V (double buffer).
-//   warp 9     MMA issuer and TMEM owner; releases a K/V stage once MMA2 and
-//              MMA4 of its chunk are done.
+//              chunk c+1 and the epilogue of chunk c overlap.  (Gated instance:
+//              O times the output gate's factor, see the gated loop below.)
+//   warp 8     TMA producer.  Passes that write outputs: Q and K and V double
+//              buffered with a barrier pair per tile (Q(c+2) once MMA3(c) is
+//              done, K(c+2) once MMA4(c) is, V(c+1) once MMA3(c) has read the
+//              state copy in its tile); state-only passes: K/V stages.
+//   warp 9     MMA issuer and TMEM owner.
+//   One count-8 barrier (SREADY) lets MMA3 go: the state warps' copy of
+//   S_{c-1} and the epilogue warps' release of O.
 // Hand-offs are mbarriers; every wait is bounded (see sm100_ptx.cuh) and a
 // timeout is recorded as GLA_ERR_TIMEOUT in the device status word.
 //
@@ -47,7 +54,10 @@
 //   V tiles      [128 tokens][dv], 128-byte swizzle, atoms of 64 dv columns
 //                (128 rows x 128 B = 16 KB).  MN-major B operand of MMA2/MMA4.
 //   S copy       [dk][dv] bf16, 128-byte swizzle, atoms of 64 dv columns
-//                (dk rows x 128 B).  MN-major B operand of MMA3.
+//                (dk rows x 128 B).  MN-major B operand of MMA3.  In the passes
+//                that write outputs it is written into the V tile of the
+//                previous chunk (smem_plan_full); in the others it has a tile
+//                of its own (smem_plan).
 #include <mutex>
 
 #include "gla_common.cuh"

@@ -22,6 +22,7 @@ int decode_step_f32(const float *, const float *, const float *, const float *, 
 int decode_step_paged_bf16(const void *, const void *, const void *, const float *, float *, const int32_t *, int,
                            void *, int, int, int, int, cudaStream_t);
 bool tc_chunk_supported(int dk, int dv, int chunk);
+bool tc_gate_supported(int dk, int dv);
 int tc_chunk_fwd_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *,
                       int, int, int, int, int, const int32_t *, cudaStream_t);
 int tc_chunk_fwd_bf16_noalloc(const void *, const void *, const void *, const float *, const float *, void *,
@@ -173,7 +174,7 @@ int gla_chunk_fwd_gated(const void *q, const void *k, const void *v, const void 
     if (rc) return rc;
     if (!aligned16(g)) return GLA_ERR_ALIGN;
     cudaStream_t st = (cudaStream_t)stream;
-    if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+    if (chunk == 128 && tc_gate_supported(dk, dv))
         return tc_chunk_fwd_gated_bf16(q, k, v, g, gate_kind, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens,
                                        st);
     return simt_chunk_fwd_gated_bf16(q, k, v, g, gate_kind, log_decay, h0, out, hT, B, T, H, dk, dv, chunk,

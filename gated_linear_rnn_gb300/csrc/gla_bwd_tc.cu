@@ -34,6 +34,8 @@
 //   MMA5   B   = dO V^T           -> scratch              mask -> P3
 //   MMA6   dQ  = P3 K + dO S^T    -> [dv+dk, dv+2dk)
 //   epilogue: row factors, bf16, stores of the rows below L.
+#include <mutex>
+
 #include "gla_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -469,6 +471,23 @@ bool tc_bwd_supported(int dk, int dv, int chunk) {
 // return at once for every other head).  Scratch: two bf16 state tiles per chunk slot.
 // With `s_images` non-null (the states before every chunk, left by the forward) the forward state pass
 // is skipped and only the gradient-state images are scratch.
+// A non-blocking stream per device for work forked off the caller's stream and joined back to it
+// before the call returns (created once; null if that failed).
+cudaStream_t side_stream() {
+    constexpr int kMaxDev = 64;
+    static std::once_flag once[kMaxDev];
+    static cudaStream_t streams[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    std::call_once(once[dev], [dev]() {
+        if (cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            streams[dev] = nullptr;
+        }
+    });
+    return streams[dev];
+}
+
 static int chunk_bwd_impl(const void *q, const void *k, const void *v, const void *dout, const float *ld, const float *h0,
                    const float *dhT, const void *s_images, void *dq, void *dk_, void *dv_, float *dh0, int nseq,
                    int Tlen, int H, int dk, int dv, const int32_t *cu, cudaStream_t st) {
@@ -495,6 +514,24 @@ static int chunk_bwd_impl(const void *q, const void *k, const void *v, const voi
     }
     const __nv_bfloat16 *s_img = s_images ? reinterpret_cast<const __nv_bfloat16 *>(s_images) : img;
     __nv_bfloat16 *g_img = img + (nimg - 1) * per;
+    // The chunked SIMT recurrences own the heads with strong decays (their CTAs of other heads return at
+    // once); they touch other heads' gradients than the tensor-core kernels, so they run on a side
+    // stream forked here and joined at the end instead of adding three launches to this stream.
+    cudaStream_t side = side_stream();
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+    bool forked = false;
+    if (side && cudaEventCreateWithFlags(&fork_ev, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&join_ev, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventRecord(fork_ev, st) == cudaSuccess && cudaStreamWaitEvent(side, fork_ev, 0) == cudaSuccess)
+        forked = true;
+    else
+        cudaGetLastError();
+    int rc_strong = GLA_OK;
+    if (forked) {
+        rc_strong = simt_chunk_bwd_bf16_strong(q, k, v, dout, ld, h0, dhT, dq, dk_, dv_, dh0, nseq, Tlen, H, dk, dv,
+                                               kC, cu, side);
+        if (cudaEventRecord(join_ev, side) != cudaSuccess) rc_strong = GLA_ERR_LAUNCH;
+    }
     int rc = s_images ? GLA_OK : tc_state_pass_bf16(k, v, ld, h0, nullptr, img, 0, nseq, Tlen, H, dk, dv, cu, st);
     if (rc == GLA_OK) rc = tc_state_pass_bf16(q, dout, ld, dhT, dh0, g_img, 1, nseq, Tlen, H, dk, dv, cu, st);
     if (rc == GLA_OK) {
@@ -522,9 +559,15 @@ static int chunk_bwd_impl(const void *q, const void *k, const void *v, const voi
             rc = cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
         }
     }
-    if (rc == GLA_OK)
+    if (forked) {
+        if (cudaStreamWaitEvent(st, join_ev, 0) != cudaSuccess && rc == GLA_OK) rc = GLA_ERR_LAUNCH;
+        if (rc == GLA_OK) rc = rc_strong;
+    } else if (rc == GLA_OK) {
         rc = simt_chunk_bwd_bf16_strong(q, k, v, dout, ld, h0, dhT, dq, dk_, dv_, dh0, nseq, Tlen, H, dk, dv, kC, cu,
                                         st);
+    }
+    if (fork_ev) cudaEventDestroy(fork_ev);
+    if (join_ev) cudaEventDestroy(join_ev);
     cudaFreeAsync(img, st);
     return rc;
 }

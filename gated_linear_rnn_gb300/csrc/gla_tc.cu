@@ -1090,44 +1090,50 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const bool full = (Lc == kC);
             for (int j = 0; j < ng; ++j) {
                 const int j0 = 64 * j;
-                uint32_t v[2][32];
-                tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
-                tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0 + 32u, v[1]);
-                // gate j has landed (in the first group the copy of gate 1 may still be in flight)
-                if (j == 0 && ng > 1)
-                    cp_async_wait_1();
-                else
-                    cp_async_wait_all();
-                __syncwarp();  // every lane's copies
-                // the gate of group j + 1 goes where group j - 1 was staged, once that store has read it
-                if (j >= 1 && j + 1 < ng) {
-                    if (lane == 0) bulk_wait_read0();
-                    __syncwarp();
-                    copy_gate(j + 1);
-                }
-                tmem_wait_ld();
-                if (j + 1 == ng) {  // last TMEM read of O for this chunk: MMA3 of the next chunk may start
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(B_SREADY));
-                }
-                // own row (lane): 64 gate values -> 64 gated outputs in place, 16-byte chunk q8 at q8 ^ (lane & 7)
                 uint8_t *myrow = smem + buf_of(j) + (uint32_t)lane * 128u;
+                // two 32-column halves (32 registers of O at a time: the gate arithmetic needs the rest)
 #pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) {
-                    uint4 *cell = reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4));
-                    const uint4 gq = *cell;
-                    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-                    const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
-                    uint32_t o2[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t f2 = gate_factor_bf16x2(gw[e], gk);
-                        const float2 ff = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&f2));
-                        o2[e] = pack_bf16x2(__uint_as_float(x[2 * e]) * grow * ff.x,
-                                            __uint_as_float(x[2 * e + 1]) * grow * ff.y);
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + kColO + (uint32_t)(j0 + 32 * hf), v);
+                    if (hf == 0) {
+                        // gate j has landed (in the first group the copy of gate 1 may still be in flight)
+                        if (j == 0 && ng > 1)
+                            cp_async_wait_1();
+                        else
+                            cp_async_wait_all();
+                        __syncwarp();  // every lane's copies
+                        // the gate of group j + 1 goes where group j - 1 was staged, once that store has read it
+                        if (j >= 1 && j + 1 < ng) {
+                            if (lane == 0) bulk_wait_read0();
+                            __syncwarp();
+                            copy_gate(j + 1);
+                        }
                     }
-                    *cell = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    tmem_wait_ld();
+                    if (j + 1 == ng && hf == 1) {  // last TMEM read of O for this chunk: MMA3 of the next may start
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(BAR(B_SREADY));
+                    }
+                    // own row (lane): 32 gate values -> 32 gated outputs in place, 16-byte chunk q8 at q8 ^ (lane & 7)
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const int q8 = 4 * hf + qq;
+                        uint4 *cell = reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4));
+                        const uint4 gq = *cell;
+                        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                        const uint32_t *x = &v[8 * qq];
+                        uint32_t o2[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t f2 = gate_factor_bf16x2(gw[e], gk);
+                            const float2 ff = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&f2));
+                            o2[e] = pack_bf16x2(__uint_as_float(x[2 * e]) * grow * ff.x,
+                                                __uint_as_float(x[2 * e + 1]) * grow * ff.y);
+                        }
+                        *cell = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    }
                 }
                 if (full) {
                     fence_async_shared();  // the staged rows must be visible to the TMA engine

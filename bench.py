@@ -58,19 +58,35 @@ def prefill_flops(B, T, H, dk, dv, C):
 
 
 def backward_flops(B, T, H, dk, dv, C):
-    """Tensor-core FLOPs issued per gla_chunk_bwd launch as full tiles (chunk C = 128): two state
-    passes (M = 128 over dk, N = dv, K = C per chunk) and, per chunk, the scores K Q^T, V dO^T,
-    dO V^T and dV = P dO + K G, dK = P Q + V G^T, dQ = P K + dO S^T.  Per token-head:
-    2 x 2 x 128 x dv + 6 C (dk + dv) + 6 dk dv."""
-    return B * T * H * (4 * 128 * dv + 6 * C * (dk + dv) + 6 * dk * dv)
+    """Tensor-core FLOPs of the chunked backward per launch, as full tiles (chunk C = 128): per chunk the
+    scores K Q^T, V dO^T, dO V^T and dV = P dO + K G, dK = P Q + V G^T, dQ = P K + dO S^T, plus the
+    chunk recurrence of the gradient state G (dk x dv per token).  Per token-head:
+    6 C (dk + dv) + 6 dk dv + 2 dk dv.  The forward state S_{c-1} recomputed by this implementation
+    (one more state pass, 2 x 128 x dv issued per token-head, M padded to 128) is not counted."""
+    return B * T * H * (6 * C * (dk + dv) + 8 * dk * dv)
 
 
-def backward_bytes(B, T, H, dk, dv, C=128):
-    """Algorithmic HBM bytes per gla_chunk_bwd launch (bf16 tensors, bf16 state tiles): the state
-    passes read k, v and q, dout; the gradient kernel reads q, k, v, dout and writes dq, dk, dv;
-    the two bf16 state tiles per chunk are written once and read once."""
-    per_token_head = 2 * 2 * (dk + dv) + 2 * 2 * (dk + dv) + 2 * (2 * dk + dv) + 8 * dk * dv // C
-    return B * T * H * per_token_head
+def backward_bytes(B, T, H, dk, dv, nseq=None, with_h0=False, with_dhT=False, with_dh0=True):
+    """The method's HBM bytes per gla_chunk_bwd launch: read q, k, v and dout (bf16), write dq, dk, dv
+    (bf16): 2 (2 dk + 2 dv) + 2 (2 dk + dv) bytes per token-head, 1,920 at dk 96, dv 192; plus the f32
+    states (h0, dhT in; dh0 out) per chain."""
+    nseq = B if nseq is None else nseq
+    st = nseq * H * dk * dv * 4
+    return (B * T * H * (2 * (2 * dk + 2 * dv) + 2 * (2 * dk + dv)) + (st if with_h0 else 0) +
+            (st if with_dhT else 0) + (st if with_dh0 else 0))
+
+
+def backward_impl_bytes(B, T, H, dk, dv, C=128):
+    """HBM bytes this implementation moves per gla_chunk_bwd launch beyond the method's own: the two state
+    passes read k, v and q, dout once more (2 (2 dk + 2 dv) per token-head), and the bf16 images of the
+    states S_{c-1} and G_c are written once and read once (8 dk dv / C per token-head)."""
+    return B * T * H * (2 * (2 * dk + 2 * dv) + 8 * dk * dv // C)
+
+
+# Datasheet HBM3e bandwidth of one GB300 (about 8 TB/s): the denominator of the decode fractions.  The
+# measured copy bandwidth (a torch tensor copy) is reported next to it; a streaming kernel such as the
+# decode step can run above that copy.
+HBM_NOMINAL_GBS = 8000.0
 
 
 def decode_bytes(N, H, dk, dv):
@@ -342,6 +358,10 @@ def run_ours(args, world, rank, local):
     sbytes, iobytes = decode_bytes(wd.B, wd.H, wd.dk, wd.dv)
     dec_avg_s = dec_total / args.steps / 1e3
 
+    # ---- the other prefill workloads: long context (segmented schedule) and the ragged packed batch ----
+    long_leg = run_prefill_workload(args, "long_bf16", stream, peaks, peak_src, dev, rank)
+    ragged_leg = run_prefill_workload(args, "ragged", stream, peaks, peak_src, dev, rank)
+
     # ---- end to end through the public API: pinned host inputs in, results back to the host ----
     e2e = run_e2e(args, P, D, w, wd, out, hT, dout, stream)
 
@@ -378,10 +398,14 @@ def run_ours(args, world, rank, local):
                                 "flops_per_launch": pflops, "peak_source": f"{peak_src} bf16 dense (burst)"}},
         "decode": {"value": sbytes / dec_avg_s / 1e9, "unit": "state GB/s",
                    "total_gbs": (sbytes + iobytes) / dec_avg_s / 1e9,
-                   "frac_of_hbm_peak": (sbytes + iobytes) / dec_avg_s / 1e9 / peaks["hbm_gbs"],
+                   "frac_of_hbm_peak": (sbytes + iobytes) / dec_avg_s / 1e9 / HBM_NOMINAL_GBS,
+                   "hbm_peak_gbs": HBM_NOMINAL_GBS, "hbm_peak_source": "GB300 datasheet HBM3e (about 8 TB/s)",
+                   "frac_of_measured_copy": (sbytes + iobytes) / dec_avg_s / 1e9 / peaks["hbm_gbs"],
                    "us_per_step": dec_avg_s * 1e6, "state_bytes": sbytes, "io_bytes": iobytes,
                    "tokens_per_s": wd.B * world / dec_avg_s},
         "e2e": e2e,
+        "prefill_long": long_leg,
+        "prefill_ragged": ragged_leg,
         "decode_paged": paged,
         "prefill_gated": gated,
         "decode_layers": layers,
@@ -399,6 +423,59 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def run_prefill_workload(args, name, stream, peaks, peak_src, dev, seed):
+    """gla_chunk_fwd on another prefill workload of the pages: ``long_bf16`` (B1 T32768 H16 with h0, the
+    segmented schedule) or ``ragged`` (64 packed sequences of U[1, 8192] tokens with per-sequence h0,
+    walked longest first).  CUDA events around every launch on the launching stream; inputs are larger
+    than L2 (no flush).  Algorithmic bytes: q, k, v read and out written once (1,152 B per token-head at
+    dk 96, dv 192) plus the f32 h0 read and hT written per chain."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    from gated_linear_rnn_gb300 import inputs as I
+    w = I.WORKLOADS[name]
+    d = I.make_prefill(w, device=dev, seed=seed)
+    cu = None if d["cu_seqlens"] is None else d["cu_seqlens"].to(dev)
+    nseq = d["q"].shape[0] if cu is None else cu.numel() - 1
+    rows = d["q"].shape[0] * d["q"].shape[1]
+    out = torch.empty(d["q"].shape[:3] + (w.dv,), dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(nseq, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+    def step():
+        gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, hT, w.chunk, cu, stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, min(args.steps, 30))
+    l0 = gla.gla_kernel_launches()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for e in ev:
+        e[0].record(stream)
+        step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    launches = (gla.gla_kernel_launches() - l0) // n
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the {name} prefill: {st_code} ({gla.gla_status_str(st_code)})")
+    times = [e[0].elapsed_time(e[1]) for e in ev]
+    us = statistics.mean(times) * 1e3
+    st_bytes = nseq * w.H * w.dk * w.dv * 4
+    by = rows * w.H * 2 * (2 * w.dk + 2 * w.dv) + (st_bytes if d["h0"] is not None else 0) + st_bytes
+    fl = prefill_flops(1, rows, w.H, w.dk, w.dv, w.chunk)
+    gbs = by / (us / 1e6) / 1e9
+    return {"value": rows / (us / 1e6), "unit": "tokens/s", "us": us, "us_median": statistics.median(times) * 1e3,
+            "us_best": min(times) * 1e3, "steps": n, "launches_per_call": launches, "tokens": rows, "sequences": nseq,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": by,
+                         "traffic": recorded_traffic(os.path.join(ROOT, "gated_linear_rnn_gb300", "csrc", "gla_tc.cu"),
+                                                     f"prefill_{name}"),
+                         "tensor": {"achieved_tflops": fl / (us / 1e6) / 1e12, "peak_tflops": peaks["bf16_tflops"],
+                                    "frac": fl / (us / 1e6) / 1e12 / peaks["bf16_tflops"], "flops_per_launch": fl}},
+            "workload": w.note, "kernel": f"gla_chunk_fwd ({name})"}
 
 
 def run_paged_decode(args, D, wd, dout, stream, peaks):
@@ -427,8 +504,9 @@ def run_paged_decode(args, D, wd, dout, stream, peaks):
     us = statistics.median(e[0].elapsed_time(e[1]) for e in ev) * 1e3
     sbytes, iobytes = decode_bytes(wd.B, wd.H, wd.dk, wd.dv)
     iobytes += wd.B * 4  # the slot table
+    gbs = (sbytes + iobytes) / (us / 1e6) / 1e9
     return {"us_per_step": us, "unit": "state GB/s", "value": sbytes / (us / 1e6) / 1e9,
-            "frac_of_hbm_peak": (sbytes + iobytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"], "steps": n,
+            "frac_of_hbm_peak": gbs / HBM_NOMINAL_GBS, "frac_of_measured_copy": gbs / peaks["hbm_gbs"], "steps": n,
             "rows": wd.B, "pool_pages": wd.B}
 
 
@@ -504,8 +582,10 @@ def run_decode_layers(args, wd, stream, peaks, dev, N=128, L=24):
         raise SystemExit(f"device status after the multi-layer decode: {st_code} ({gla.gla_status_str(st_code)})")
     sbytes, iobytes = decode_bytes(N * L, H, dk, dv)
     us = res["one_launch"]
+    gbs = (sbytes + iobytes) / (us / 1e6) / 1e9
     return {"us_one_launch": us, "us_per_layer_launches": res["per_layer"], "unit": "state GB/s",
-            "value": sbytes / (us / 1e6) / 1e9, "frac_of_hbm_peak": (sbytes + iobytes) / (us / 1e6) / 1e9 / peaks["hbm_gbs"],
+            "value": sbytes / (us / 1e6) / 1e9, "frac_of_hbm_peak": gbs / HBM_NOMINAL_GBS,
+            "frac_of_measured_copy": gbs / peaks["hbm_gbs"],
             "sequences": N, "layers": L, "pool_bytes": pool.numel() * 4}
 
 
@@ -579,7 +659,8 @@ def run_backward(args, P, w, stream, peaks, peak_src):
         raise SystemExit(f"device status after the backward: {st_code} ({gla.gla_status_str(st_code)})")
     ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     fl = backward_flops(w.B, w.T, w.H, w.dk, w.dv, w.chunk)
-    by = backward_bytes(w.B, w.T, w.H, w.dk, w.dv, w.chunk)
+    by = backward_bytes(w.B, w.T, w.H, w.dk, w.dv)
+    impl = backward_impl_bytes(w.B, w.T, w.H, w.dk, w.dv, w.chunk)
     gbs = by / (ms / 1e3) / 1e9
     tfl = fl / (ms / 1e3) / 1e12
     return {"value": w.B * w.T / (ms / 1e3), "unit": "tokens/s", "ms": ms, "launches_per_call": launches,
@@ -587,6 +668,10 @@ def run_backward(args, P, w, stream, peaks, peak_src):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy bandwidth",
                          "algorithmic_bytes_per_launch": by,
+                         "algorithmic_bytes_note": "q, k, v, dout read and dq, dk, dv written once (bf16): "
+                                                   "1,920 B per token-head, plus dh0",
+                         "implementation_extra_bytes_per_launch": impl,
+                         "moved_gbs_incl_implementation": (by + impl) / (ms / 1e3) / 1e9,
                          "tensor": {"achieved_tflops": tfl, "peak_tflops": peaks["bf16_tflops"],
                                     "frac": tfl / peaks["bf16_tflops"], "flops_per_launch": fl}},
             "kernel": "gla_chunk_bwd (layer_bf16): two tensor-core state passes + chunk-parallel gradient kernel"}
@@ -692,8 +777,9 @@ def run_e2e(args, P, D, w, wd, out, hT, dout, stream):
 
 
 def run_only(args):
-    """W + K back-to-back calls of one operation (the backward of the layer workload, or the conv over
-    B8 T2048 D3072), then a device-status check: a fixed command line to put under a profiler."""
+    """W + K back-to-back calls of one operation (the backward of the layer workload, the conv over
+    B8 T2048 D3072, or the forward of a prefill workload), then a device-status check: a fixed command
+    line to put under a profiler."""
     import torch
     from gated_linear_rnn_gb300 import build as Bld
     from gated_linear_rnn_gb300 import gla
@@ -705,7 +791,17 @@ def run_only(args):
     Bld.build_library()
     gla.load()
     w = I.WORKLOADS["layer_bf16"]
-    if args.only == "backward":
+    if args.only in ("layer", "long", "ragged"):
+        wp = I.WORKLOADS["layer_bf16" if args.only == "layer" else "long_bf16" if args.only == "long" else "ragged"]
+        d = I.make_prefill(wp, device=dev, seed=0)
+        cu = None if d["cu_seqlens"] is None else d["cu_seqlens"].to(dev)
+        nseq = d["q"].shape[0] if cu is None else cu.numel() - 1
+        out = torch.empty(d["q"].shape[:3] + (wp.dv,), dtype=torch.bfloat16, device=dev)
+        hT = torch.empty(nseq, wp.H, wp.dk, wp.dv, dtype=torch.float32, device=dev)
+
+        def call():
+            gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, hT, wp.chunk, cu)
+    elif args.only == "backward":
         d = I.make_backward(w, device=dev, seed=0, dhT_std=0.0)
         dq, dk, dv = (torch.empty_like(d[k]) for k in ("q", "k", "v"))
 
@@ -736,9 +832,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-steps", type=int, default=5, help="timed launches of the backward (0: skip)")
-    ap.add_argument("--only", choices=["backward", "conv"], default=None,
-                    help="run just W + K calls of one operation on its bench workload (for profilers); "
-                         "prints one status line, not the bench line")
+    ap.add_argument("--only", choices=["backward", "conv", "layer", "long", "ragged"], default=None,
+                    help="run just W + K calls of one operation on its bench workload (for profilers): the "
+                         "layer backward, the conv, or the forward of the layer, long-context or ragged "
+                         "workload; prints one status line, not the bench line")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of fp64 reference work to time")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -58,6 +58,7 @@
 //                that write outputs it is written into the V tile of the
 //                previous chunk (smem_plan_full); in the others it has a tile
 //                of its own (smem_plan).
+#include <atomic>
 #include <mutex>
 
 #include "gla_common.cuh"
@@ -126,7 +127,7 @@ struct Smem {
 };
 
 // Barriers, lookup tables and the TMEM slot after the tiles at offset `at`.
-__host__ __device__ inline void smem_plan_tail(Smem &p, uint32_t at) {
+__host__ __device__ constexpr void smem_plan_tail(Smem &p, uint32_t at) {
     p.xp = at;                   // output staging: 4 warps x 32 rows x 128 B
     p.tab = p.xp + 4u * 4096u;
     p.utab = p.tab + 132 * 4;
@@ -137,8 +138,8 @@ __host__ __device__ inline void smem_plan_tail(Smem &p, uint32_t at) {
     p.total = p.abort + 4;
 }
 
-__host__ __device__ inline Smem smem_plan(int dk, int dv) {
-    Smem p;
+__host__ __device__ constexpr Smem smem_plan(int dk, int dv) {
+    Smem p{};
     const uint32_t qk = (uint32_t)(dk / 32) * 8192u;
     const uint32_t vv = (uint32_t)(dv / 64) * 16384u;
     p.q = 0;
@@ -157,8 +158,8 @@ __host__ __device__ inline Smem smem_plan(int dk, int dv) {
 // current one is still read, and no state-copy tile of its own.  The bf16 copy of S_{c-1} that MMA3(c)
 // reads is written into the V tile of chunk c-1 (free once MMA2(c-1) and MMA4(c-1) are done; dk <= 128
 // rows of dv bf16 fit in its 128 rows), and V(c+1) lands there once MMA3(c) has read it.
-__host__ __device__ inline Smem smem_plan_full(int dk, int dv, bool gate = false) {
-    Smem p;
+__host__ __device__ constexpr Smem smem_plan_full(int dk, int dv, bool gate = false) {
+    Smem p{};
     const uint32_t qk = (uint32_t)(dk / 32) * 8192u;
     const uint32_t vv = (uint32_t)(dv / 64) * 16384u;
     p.q = 0;
@@ -1296,6 +1297,30 @@ int plan_segments(int nseq, int H, int Tlen, const int32_t *cu, int *seg_chunks)
     return (nck + *seg_chunks - 1) / *seg_chunks;
 }
 
+// Bytes of segment-state scratch the segmented schedule takes: the end states from zero and the start
+// states, each [chains, nseg - 1, dk, dv] f32.  plan_segments keeps chains * nseg <= SMs, so this is at
+// most 2 * (SMs - chains) * dk * dv * 4 < 2 * SMs * dk * dv * 4.
+constexpr long long seg_scratch_bytes(long long chains, int nseg, int dk, int dv) {
+    return nseg > 1 ? 2LL * chains * (nseg - 1) * dk * dv * 4 : 0;
+}
+
+// The largest state (dk * dv) among the head sizes the tensor-core forward takes: dk a multiple of 32 up to
+// 128, dv a multiple of 64 up to 192, both shared-memory plans within the 227 KB a CTA may opt in to.
+constexpr long long max_tc_state_elems() {
+    long long best = 0;
+    for (int dk = 32; dk <= 128; dk += 32)
+        for (int dv = 64; dv <= 192; dv += 64)
+            if (smem_plan(dk, dv).total + 1024 <= 232448u && smem_plan_full(dk, dv).total + 1024 <= 232448u &&
+                (long long)dk * dv > best)
+                best = (long long)dk * dv;
+    return best;
+}
+// The no-alloc forward's fixed array holds the segment states of every problem the tensor-core kernel takes
+// on a GB300 (152 SMs, at least one chain): GLA_ERR_SCRATCH_LIMIT is never returned there.
+static_assert(max_tc_state_elems() == 96 * 192, "the largest tensor-core state is 96 x 192");
+static_assert(seg_scratch_bytes(1, 152, 96, 192) <= (long long)GLA_NOALLOC_SCRATCH_BYTES,
+              "the no-alloc scratch array must hold the segment states of one chain cut over 152 SMs");
+
 // A third K/V stage takes the Q buffer (same size as a K tile) and the state copy plus the output
 // staging space for its V tile.
 bool three_stages_fit(int dk, int dv) {
@@ -1503,28 +1528,39 @@ static __device__ __align__(256) float g_noalloc_scratch[GLA_NOALLOC_SCRATCH_BYT
 
 namespace {
 constexpr int kMaxDev = 64;
-std::once_flag g_scratch_once[kMaxDev];
-float *g_scratch_ptr[kMaxDev];
-cudaError_t g_scratch_err[kMaxDev];
+std::mutex g_scratch_mu;
+std::atomic<float *> g_scratch_ptr[kMaxDev];  // set once a lookup on that device has succeeded
 
-// Device address of the scratch array on the current device, looked up once per device.
+// Device address of the scratch array on the current device.  A successful lookup is kept for the
+// process; a failed one is not: its CUDA error is cleared (so that no later, unrelated call reports it)
+// and the next call tries again.  With lazy module loading the lookup is what loads this file's kernels
+// and the array onto the device when no other entry point has, so it can fail for want of memory:
+// that is GLA_ERR_NOMEM, any other failure GLA_ERR_LAUNCH.
 float *noalloc_scratch(int *err) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        cudaGetLastError();
         *err = GLA_ERR_LAUNCH;
         return nullptr;
     }
-    std::call_once(g_scratch_once[dev], [dev]() {
-        void *p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_scratch_ptr[dev] = g_scratch_err[dev] == cudaSuccess ? static_cast<float *>(p) : nullptr;
-    });
-    if (g_scratch_err[dev] != cudaSuccess || g_scratch_ptr[dev] == nullptr) {
-        *err = GLA_ERR_LAUNCH;
-        return nullptr;
+    float *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            void *addr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+            if (e != cudaSuccess || addr == nullptr) {
+                cudaGetLastError();
+                *err = (e == cudaErrorMemoryAllocation) ? GLA_ERR_NOMEM : GLA_ERR_LAUNCH;
+                return nullptr;
+            }
+            p = static_cast<float *>(addr);
+            g_scratch_ptr[dev].store(p, std::memory_order_release);
+        }
     }
     *err = GLA_OK;
-    return g_scratch_ptr[dev];
+    return p;
 }
 }  // namespace
 
@@ -1538,7 +1574,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
     if (nseg == 1) return tc_chunk_fwd_bf16(q, k, v, ld, h0, out, hT, nseq, Tlen, H, dk, dv, cu, st);  // no scratch
     const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
-    if (2 * per * sizeof(float) > (size_t)GLA_NOALLOC_SCRATCH_BYTES) return GLA_ERR_SCRATCH_LIMIT;
+    if (seg_scratch_bytes(chains, nseg, dk, dv) > (long long)GLA_NOALLOC_SCRATCH_BYTES) return GLA_ERR_SCRATCH_LIMIT;
     int err = GLA_OK;
     float *scratch = noalloc_scratch(&err);
     if (!scratch) return err;

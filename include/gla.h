@@ -146,11 +146,19 @@ GLA_API int gla_chunk_fwd_gated(const void *q, const void *k, const void *v, con
  * every device that loads the library, until the process exits) instead of
  * memory taken with cudaMallocAsync.  The call itself never allocates or frees
  * device memory.  A problem whose segment states need more than that array is
- * rejected with GLA_ERR_SCRATCH_LIMIT before anything is launched (at most
- * 2 * min(SMs, 2 * chains) * dk * dv * 4 bytes are needed; every shape the
- * tensor-core kernel takes fits on a GPU with up to 170 SMs).
+ * rejected with GLA_ERR_SCRATCH_LIMIT before anything is launched.  The
+ * segment states take 2 * chains * (nseg - 1) * dk * dv * 4 bytes, where
+ * chains = B * H and the schedule keeps chains * nseg <= SMs, so at most
+ * 2 * (SMs - chains) * dk * dv * 4 bytes: every shape the tensor-core kernel
+ * takes (largest state 96 x 192) fits on a GB300 (152 SMs), so the limit is
+ * never hit there.
  *
- * The first call on each device looks up that device's address of the array
+ * The array is placed on a device when the library's forward kernels are
+ * loaded onto it.  With CUDA's lazy module loading (the default) that is the
+ * first call on that device of any entry point using them, not the moment the
+ * library is loaded; if that first call is this one and the device has no
+ * room left, it returns GLA_ERR_NOMEM (and a later call tries again).  The
+ * first call on each device also looks up that device's address of the array
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * All calls share the one array and every launch overwrites the parts it reads,
  * so nothing carries over between calls, but calls whose work overlaps on the

@@ -107,9 +107,9 @@ def test_backward_is_deterministic():
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
-def test_backward_layer_workload_sampled():
-    """The layer workload at full size (B8 T2048 H16 dk96 dv192), four chains checked against the reference."""
-    check_backward(I.WORKLOADS["layer_bf16"], units=[(0, 0), (3, 7), (5, 12), (7, 15)], seed=1)
+def test_backward_layer_workload_full_size():
+    """The layer workload at full size (B8 T2048 H16 dk96 dv192): every chain's dq, dk, dv and dh0."""
+    check_backward(I.WORKLOADS["layer_bf16"], seed=1)
 
 
 def test_backward_matches_forward_linearisation():

@@ -65,7 +65,13 @@ def test_algorithmic_counts():
 
 def test_backward_counts():
     import bench
-    # state passes read k, v and q, dout; the gradient kernel reads q, k, v, dout and writes dq, dk, dv;
-    # two bf16 96 x 192 state tiles per 128-token chunk, written and read once: 4,224 B per token-head
-    assert bench.backward_bytes(1, 1, 1, 96, 192) == 4 * 288 + 4 * 288 + 2 * 384 + 8 * 96 * 192 // 128 == 4224
-    assert bench.backward_flops(1, 1, 1, 96, 192, 128) == 4 * 128 * 192 + 6 * 128 * 288 + 6 * 96 * 192
+    # the method's bytes: q, k, v, dout read and dq, dk, dv written once in bf16, 1,920 B per token-head at
+    # dk = 96, dv = 192; dh0 (f32) per chain
+    assert bench.backward_bytes(1, 1, 1, 96, 192, with_dh0=False) == 2 * (2 * 96 + 2 * 192) + 2 * (2 * 96 + 192) == 1920
+    assert bench.backward_bytes(8, 2048, 16, 96, 192) == 8 * 2048 * 16 * 1920 + 8 * 16 * 96 * 192 * 4
+    # what this implementation moves on top: the state passes' second read of q, k, v, dout and the bf16
+    # state images (two 96 x 192 tiles per 128-token chunk, written and read once)
+    assert bench.backward_impl_bytes(1, 1, 1, 96, 192) == 2 * 576 + 8 * 96 * 192 // 128 == 2304
+    # FLOPs of the chunked backward: six score / gradient contractions over the chunk plus the three
+    # inter-chunk terms and the gradient-state recurrence
+    assert bench.backward_flops(1, 1, 1, 96, 192, 128) == 6 * 128 * 288 + 8 * 96 * 192

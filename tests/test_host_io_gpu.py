@@ -77,19 +77,17 @@ def test_host_forward_pageable_memory_and_no_states():
 
 def test_host_forward_layer_workload_eight_groups():
     """B8 T2048 H16 dk96 dv192: 39 MB of copies per sequence, so every sequence is its own group.
-    Each group must equal the device entry point on that one sequence bit for bit, and sampled
-    chains must match the reference."""
+    Each group must equal the device entry point on that one sequence bit for bit, and every chain
+    must match the reference."""
     w = I.WORKLOADS["layer_bf16"]
     d = I.make_prefill(w, device="cuda", seed=6)
     out, hT = host_forward(d, 128)
     for b in (0, 3, 7):
         od, hd = device_forward(d, 128, b, b + 1)
         assert torch.equal(out[b:b + 1], od) and torch.equal(hT[b:b + 1], hd), b
-    units = [(0, 0), (4, 9), (7, 15)]
-    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], units=units)
-    for s, h in units:
-        assert oracle.rel_err(out[s, :, h].float().numpy(), o_ref[s, :, h]) <= 1e-2, (s, h)
-        assert oracle.rel_err(hT[s, h].numpy(), h_ref[s, h]) <= 1e-2, (s, h)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(out.float().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.numpy(), h_ref) <= 1e-2
 
 
 def test_host_forward_rejects_device_tensors():

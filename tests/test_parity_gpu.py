@@ -38,12 +38,31 @@ def with_dev_cu(d):
     return d
 
 
+def rel_err_rows(got, ref, rows=4096):
+    """max|got - ref| / max|ref| over the whole tensor, taken over blocks of the token axis (a full-size
+    output widened to float64 in one piece would need several times the host memory)."""
+    num = den = 0.0
+    for a in range(0, ref.shape[1], rows):
+        g = got[:, a:a + rows].float().cpu().numpy().astype(np.float64)
+        r = ref[:, a:a + rows]
+        num = max(num, float(np.max(np.abs(g - r))))
+        den = max(den, float(np.max(np.abs(r))))
+    return num / den if den else num
+
+
 def check_prefill(w, chunk=None, units=None, seed=0, **kw):
     d = with_dev_cu(I.make_prefill(w, device="cuda", seed=seed, **kw))
     chunk = chunk or w.chunk
     out, hT = run_prefill(d, chunk)
     o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"],
                                     cu_seqlens=d["cu_seqlens"], units=units)
+    if units is None and o_ref.size > (1 << 26):
+        # full-size workloads: every chain, element by element, compared block by block
+        eo, eh = rel_err_rows(out, o_ref), oracle.rel_err(hT.cpu().numpy(), h_ref)
+        tol = TOL[w.dtype]
+        assert eo <= tol and eh <= tol, f"out {eo:.3e} hT {eh:.3e} (tol {tol})"
+        assert torch.isfinite(out).all() and torch.isfinite(hT).all()
+        return eo, eh
     o = out.float().cpu().numpy()
     h = hT.cpu().numpy()
     if units is not None:
@@ -292,24 +311,21 @@ def test_decode_workload_full_size():
     assert oracle.rel_err(d["state"].cpu().numpy(), s_ref) <= 1e-2
 
 
-# ---- full-size workloads, sampled chains ----
+# ---- full-size workloads: every chain of the workload against the reference ----
 def test_layer_workload_full_size():
-    w = I.WORKLOADS["layer_bf16"]
-    units = [(b, h) for b in range(8) for h in range(16)]
-    check_prefill(w, units=units)
+    """B8 T2048 H16 dk96 dv192, the launch the benchmark times: all 128 chains."""
+    check_prefill(I.WORKLOADS["layer_bf16"])
 
 
-def test_long_workload_full_size_sampled():
-    w = I.WORKLOADS["long_bf16"]
-    check_prefill(w, units=[(0, 0), (0, 5), (0, 15)])
+def test_long_workload_full_size():
+    """B1 T32768 H16 with h0 ~ N(0, 0.02^2) (segmented schedule): all 16 heads, every token."""
+    check_prefill(I.WORKLOADS["long_bf16"])
 
 
-def test_ragged_workload_full_size_sampled():
-    w = I.WORKLOADS["ragged"]
-    lengths = I.ragged_lengths(w.ragged_n, w.ragged_max, 0)
-    order = torch.argsort(lengths)
-    units = [(int(order[0]), 0), (int(order[-1]), 15), (int(order[31]), 7), (3, 3)]
-    check_prefill(w, units=units)
+def test_ragged_workload_full_size():
+    """64 packed sequences of U[1, 8192] tokens with per-sequence h0, walked longest first: every
+    (sequence, head) chain, every token and every final state."""
+    check_prefill(I.WORKLOADS["ragged"])
 
 
 # ---- errors recorded on the device ----

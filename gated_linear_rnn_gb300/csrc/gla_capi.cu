@@ -90,6 +90,12 @@ const DeviceInfo &device_info() {
     return g_info[dev];
 }
 
+// Chunk lengths the tensor-core kernels serve: 128, and 64 as two 64-token chunks per 128-row tile.  In
+// such a tile the second chunk's carried-state term through the first chunk's keys and values is the
+// tile's lower-left attention block, i.e. the chunk-64 recurrence without rounding the state between the
+// two chunks to bf16: the same map up to rounding.
+bool tc_chunk_len(int chunk) { return chunk == 64 || chunk == 128; }
+
 namespace {
 
 int check_decays_and_sizes(const float *log_decay, int B, int T, int H, int dk, int dv) {
@@ -160,7 +166,7 @@ int gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_
     int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+    if (tc_chunk_len(chunk) && tc_chunk_supported(dk, dv, 128))
         return tc_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens, st);
     return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
 }
@@ -174,7 +180,7 @@ int gla_chunk_fwd_gated(const void *q, const void *k, const void *v, const void 
     if (rc) return rc;
     if (!aligned16(g)) return GLA_ERR_ALIGN;
     cudaStream_t st = (cudaStream_t)stream;
-    if (chunk == 128 && tc_gate_supported(dk, dv))
+    if (tc_chunk_len(chunk) && tc_gate_supported(dk, dv))
         return tc_chunk_fwd_gated_bf16(q, k, v, g, gate_kind, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens,
                                        st);
     return simt_chunk_fwd_gated_bf16(q, k, v, g, gate_kind, log_decay, h0, out, hT, B, T, H, dk, dv, chunk,
@@ -187,7 +193,7 @@ int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const flo
     int rc = check_prefill(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    if (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+    if (tc_chunk_len(chunk) && tc_chunk_supported(dk, dv, 128))
         return tc_chunk_fwd_bf16_noalloc(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, cu_seqlens, st);
     // the SIMT kernel takes no scratch
     return simt_chunk_fwd_bf16(q, k, v, log_decay, h0, out, hT, B, T, H, dk, dv, chunk, cu_seqlens, st);
@@ -220,7 +226,7 @@ int gla_chunk_bwd(const void *q, const void *k, const void *v, const void *dout,
                   int H, int dk, int dv, int chunk, const int32_t *cu_seqlens, void *stream) {
     int rc = check_backward(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, cu_seqlens);
     if (rc) return rc;
-    if (chunk == 128 && tc_bwd_supported(dk, dv, chunk))
+    if (tc_chunk_len(chunk) && tc_bwd_supported(dk, dv, 128))
         return tc_chunk_bwd_bf16(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv,
                                  cu_seqlens, (cudaStream_t)stream);
     return simt_chunk_bwd_bf16(q, k, v, dout, log_decay, h0, dhT, dq, dk_out, dv_out, dh0, B, T, H, dk, dv, chunk,
@@ -240,7 +246,7 @@ int gla_chunk_fwd_save(const void *q, const void *k, const void *v, const float 
     if (rc) return rc;
     if (!state_images) return GLA_ERR_ARG;
     if (!aligned16(state_images)) return GLA_ERR_ALIGN;
-    if (!(chunk == 128 && tc_bwd_supported(dk, dv, chunk))) return GLA_ERR_UNSUPPORTED;
+    if (!(tc_chunk_len(chunk) && tc_bwd_supported(dk, dv, 128))) return GLA_ERR_UNSUPPORTED;
     return tc_chunk_fwd_bf16_save(q, k, v, log_decay, h0, out, hT, state_images, B, T, H, dk, dv, cu_seqlens,
                                   (cudaStream_t)stream);
 }
@@ -253,7 +259,7 @@ int gla_chunk_bwd_saved(const void *q, const void *k, const void *v, const void 
     if (rc) return rc;
     if (!state_images) return GLA_ERR_ARG;
     if (!aligned16(state_images)) return GLA_ERR_ALIGN;
-    if (!(chunk == 128 && tc_bwd_supported(dk, dv, chunk))) return GLA_ERR_UNSUPPORTED;
+    if (!(tc_chunk_len(chunk) && tc_bwd_supported(dk, dv, 128))) return GLA_ERR_UNSUPPORTED;
     return tc_chunk_bwd_bf16_saved(q, k, v, dout, log_decay, h0, dhT, state_images, dq, dk_out, dv_out, dh0, B, T, H,
                                    dk, dv, cu_seqlens, (cudaStream_t)stream);
 }
@@ -382,6 +388,19 @@ const char *gla_status_str(int status) {
         case GLA_ERR_SCRATCH_LIMIT: return "problem needs more segment-state scratch than the fixed no-alloc array";
         default: return "unknown status";
     }
+}
+
+int gla_chunk_kernel(int op, int dtype, int dk, int dv, int chunk) {
+    if (op != GLA_OP_FORWARD && op != GLA_OP_FORWARD_GATED && op != GLA_OP_BACKWARD) return GLA_ERR_ARG;
+    if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_ARG;
+    if (dk < 16 || dk > 256 || dv < 16 || dv > 512 || dk % 8 || dv % 8) return GLA_ERR_UNSUPPORTED;
+    if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return GLA_ERR_UNSUPPORTED;
+    if (!device_info().ok) return GLA_ERR_UNSUPPORTED;
+    if (dtype == GLA_F32 || !tc_chunk_len(chunk)) return GLA_KERNEL_SIMT;
+    const bool tc = op == GLA_OP_FORWARD         ? tc_chunk_supported(dk, dv, 128)
+                    : op == GLA_OP_FORWARD_GATED ? tc_gate_supported(dk, dv)
+                                                 : tc_bwd_supported(dk, dv, 128);
+    return tc ? GLA_KERNEL_TENSOR_CORE : GLA_KERNEL_SIMT;
 }
 
 uint64_t gla_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

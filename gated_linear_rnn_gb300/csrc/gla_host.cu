@@ -17,6 +17,7 @@ int tc_chunk_fwd_bf16(const void *, const void *, const void *, const float *, c
 int simt_chunk_fwd_bf16(const void *, const void *, const void *, const float *, const float *, void *, float *, int,
                         int, int, int, int, int, const int32_t *, cudaStream_t);
 bool tc_chunk_supported(int dk, int dv, int chunk);
+bool tc_chunk_len(int chunk);
 
 namespace {
 
@@ -106,7 +107,7 @@ int chunk_fwd_host_bf16(const void *q, const void *k, const void *v, const float
         // compute on the caller's stream
         if (rc == GLA_OK && cudaStreamWaitEvent(st, ev_in[g], 0) != cudaSuccess) rc = GLA_ERR_LAUNCH;
         if (rc == GLA_OK) {
-            rc = (chunk == 128 && tc_chunk_supported(dk, dv, chunk))
+            rc = (tc_chunk_len(chunk) && tc_chunk_supported(dk, dv, 128))
                      ? tc_chunk_fwd_bf16(qd, kd, vd, ld_d, h0 ? h0d : nullptr, od, hT ? hTd : nullptr, nb, T, H,
                                          dk, dv, nullptr, st)
                      : simt_chunk_fwd_bf16(qd, kd, vd, ld_d, h0 ? h0d : nullptr, od, hT ? hTd : nullptr, nb, T,

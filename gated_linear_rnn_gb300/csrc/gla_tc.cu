@@ -210,6 +210,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// The four contractions as groups of K-steps of 16, fully unrolled, with every operand descriptor advanced
+// by a constant from a base computed once: the MMA warp spends a few instructions per tcgen05.mma, so the
+// tensor pipe is not left waiting for it to issue.  A descriptor holds its start address in 16-byte units,
+// so a byte offset o adds o >> 4 (shared-memory offsets stay below 256 KB: no carry out of the field).
+// Q, K tiles (K-major, 64B swizzle): K-step kk is 32 bytes into atom kk / 2 (8 KB apart).
+__device__ __forceinline__ uint64_t qk_step(int kk) { return (uint64_t)((kk >> 1) * 512 + (kk & 1) * 2); }
+
+// MMA1: A = Q K^T (ksteps = dk / 16 <= 8), both operands K-major.
+__device__ __forceinline__ void mma_group_qk(uint32_t d, uint64_t dq, uint64_t dk_, uint32_t id, int ksteps) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        if (kk < ksteps) mma_ss(d, dq + qk_step(kk), dk_ + qk_step(kk), id, kk > 0);
+}
+// MMA3: O = Q S; B = the bf16 state copy, MN-major, 2 KB per K-step of 16 dk rows.
+__device__ __forceinline__ void mma_group_qs(uint32_t d, uint64_t dq, uint64_t ds, uint32_t id, int ksteps) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        if (kk < ksteps) mma_ss(d, dq + qk_step(kk), ds + (uint64_t)(kk * 128), id, kk > 0);
+}
+// MMA2: O += P V; A = P in TMEM (8 columns per K-step of 16 tokens), B = V MN-major (2 KB per K-step).
+__device__ __forceinline__ void mma_group_pv(uint32_t d, uint32_t p_tmem, uint64_t dv_, uint32_t id) {
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) mma_ts(d, p_tmem + (uint32_t)(kk * 8), dv_ + (uint64_t)(kk * 128), id, 1);
+}
+// MMA4: S += K~^T V; A = K tile read MN-major (1 KB per K-step of 16 tokens), B = V MN-major.
+__device__ __forceinline__ void mma_group_kv(uint32_t d, uint64_t dkt, uint64_t dv_, uint32_t id) {
+#pragma unroll
+    for (int kk = 0; kk < kC / 16; ++kk) mma_ss(d, dkt + (uint64_t)(kk * 64), dv_ + (uint64_t)(kk * 128), id, 1);
+}
+// Base descriptors of the operand roles.
+__device__ __forceinline__ uint64_t desc_qk(uint32_t a) { return smem_desc(a, 16, 512, kSwizzle64B); }
+__device__ __forceinline__ uint64_t desc_kt(uint32_t a) { return smem_desc(a, 8192, 512, kSwizzle64B); }
+__device__ __forceinline__ uint64_t desc_v(uint32_t a) { return smem_desc(a, 16384, 1024, kSwizzle128B); }
+__device__ __forceinline__ uint64_t desc_s(uint32_t a, int dk) { return smem_desc(a, (uint32_t)dk * 128u, 1024, kSwizzle128B); }
+
 // Multiply the 16-byte chunk at `p` (8 bf16) by f, in place.
 __device__ __forceinline__ void scale_chunk_bf16(uint8_t *p, float f) {
     uint4 x = *reinterpret_cast<uint4 *>(p);
@@ -474,6 +509,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint32_t id_pv = idesc_bf16(kC, dv, 0, 1);
             const uint32_t id_kv = idesc_bf16(kC, dv, 1, 1);
             const int ksteps_dk = dk / 16;
+            // operand descriptors of the full passes' tiles (the state copy of chunk c sits in the V tile
+            // of chunk c - 1)
+            const uint64_t dq0 = desc_qk(sbase + o_q), dq1 = desc_qk(sbase + o_q1);
+            const uint64_t dk0 = desc_qk(sbase + o_k0), dk1 = desc_qk(sbase + o_k1);
+            const uint64_t dkt0 = desc_kt(sbase + o_k0), dkt1 = desc_kt(sbase + o_k1);
+            const uint64_t dv0 = desc_v(sbase + o_v0), dv1 = desc_v(sbase + o_v1);
+            const uint64_t ds_in_v0 = desc_s(sbase + o_v0, dk), ds_in_v1 = desc_s(sbase + o_v1, dk);
             // image of the state before chunk 0 of this chain (slot start / 128 + seq; chunk c adds c slots)
             // image slot of the state before this segment's first chunk (sequence slot start / 128 + seq,
             // plus the segment's first chunk)
@@ -493,10 +535,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                          mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);
                     if (!ok) break;
                     tc_fence_after();
-                    for (int kk = 0; kk < kC / 16; ++kk) {
-                        mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
-                               smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
-                    }
+                    mma_group_kv(tmem + kColS, desc_kt(kbuf), desc_v(vbuf), id_kv);
                     mma_commit(BAR(B_SFULL));
                     mma_commit(BAR(b_kvempty(s)));
                     // the image of the state before this chunk: copy it out while the MMA runs
@@ -515,10 +554,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                          (m != 0 || mbar_wait(BAR(B_SREADY), (c / nblk) & 1, abort_flag, kWaitBudgetNs));
                     if (!ok) break;
                     tc_fence_after();
-                    for (int kk = 0; kk < kC / 16; ++kk) {
-                        mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
-                               smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
-                    }
+                    mma_group_kv(tmem + kColS, desc_kt(kbuf), desc_v(vbuf), id_kv);
                     mma_commit(BAR(b_kvempty(s)));
                     if (block_end) mma_commit(BAR(B_SFULL));
                     continue;
@@ -538,17 +574,16 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         bulk_commit();
                         bulk_wait_read0();
                     }
-                    for (int kk = 0; kk < kC / 16; ++kk) {
-                        mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
-                               smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
-                    }
+                    mma_group_kv(tmem + kColS, desc_kt(kbuf), desc_v(vbuf), id_kv);
                     mma_commit(BAR(B_SFULL));
                     mma_commit(BAR(b_kvempty(s)));
                     continue;
                 }
                 // full passes: MMA1(c), MMA3(c), MMA2(c), MMA4(c).  MMA4 last: the state pass of the next
                 // chunk waits for it and then writes its copy into V tile c, which MMA2 has read by then.
-                const uint32_t qbuf = sbase + qbuf_of(c), sbuf = sbase + scopy_of(c);
+                const uint64_t dq = (c & 1) ? dq1 : dq0, dkk = s ? dk1 : dk0, dkt = s ? dkt1 : dkt0;
+                const uint64_t dvv = s ? dv1 : dv0, dss = (c & 1) ? ds_in_v0 : ds_in_v1;
+                const uint32_t sbuf = sbase + scopy_of(c);
                 const uint32_t ph = (uint32_t)(c >> 1) & 1u;  // phase of chunk c on its Q tile and K/V stage
                 // (factored form: KPREP implies that K has landed)
                 ok = mbar_wait(BAR(s ? B_QFULL1 : B_QFULL), ph, abort_flag, kWaitBudgetNs) &&
@@ -557,11 +592,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 // MMA1: A = Q K^T, K'' in the factored form (both K-major, 64B swizzle; 2 K-steps per atom)
-                for (int kk = 0; kk < ksteps_dk; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 1) * 8192u + (uint32_t)(kk & 1) * 32u;
-                    mma_ss(tmem + kColA, smem_desc(qbuf + off, 16, 512, kSwizzle64B),
-                           smem_desc(kbuf + off, 16, 512, kSwizzle64B), id_qk, kk > 0);
-                }
+                mma_group_qk(tmem + kColA, dq, dkk, id_qk, ksteps_dk);
                 mma_commit(BAR(B_AFULL));
                 ok = mbar_wait(BAR(B_SREADY), c & 1, abort_flag, kWaitBudgetNs);  // copy S_{c-1} ready, O free
                 if (!ok) break;
@@ -572,12 +603,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 // MMA3: O = Q S_{c-1} (factored) or Q' S_{c-1} (direct); A K-major 64B swizzle,
                 // B = S copy, MN-major 128B swizzle
-                for (int kk = 0; kk < ksteps_dk; ++kk) {
-                    const uint32_t aoff = (uint32_t)(kk >> 1) * 8192u + (uint32_t)(kk & 1) * 32u;
-                    mma_ss(tmem + kColO, smem_desc(qbuf + aoff, 16, 512, kSwizzle64B),
-                           smem_desc(sbuf + (uint32_t)kk * 2048u, (uint32_t)dk * 128u, 1024, kSwizzle128B), id_qs,
-                           kk > 0);
-                }
+                mma_group_qs(tmem + kColO, dq, dss, id_qs, ksteps_dk);
                 mma_commit(BAR(s ? B_QEMPTY1 : B_QEMPTY));    // Q(c+2) may land in this Q tile
                 mma_commit(BAR(s ? B_VEMPTY0 : B_VEMPTY1));   // V(c+1) may land over the copy S_{c-1}
                 ok = mbar_wait(BAR(s ? B_VFULL1 : B_VFULL0), ph, abort_flag, kWaitBudgetNs) &&
@@ -585,10 +611,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 // MMA2: O += P V (A = P in TMEM, 8 columns per K-step of 16 tokens)
-                for (int kk = 0; kk < kC / 16; ++kk) {
-                    mma_ts(tmem + kColO, tmem + kColA + (uint32_t)kk * 8u,
-                           smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_pv, 1);
-                }
+                mma_group_pv(tmem + kColO, tmem + kColA, dvv, id_pv);
                 mma_commit(BAR(B_OFULL));
                 if (!fact) {
                     ok = mbar_wait(BAR(b_kprep(s)), ph, abort_flag, kWaitBudgetNs);
@@ -596,10 +619,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tc_fence_after();
                 }
                 // MMA4: S += K~^T V (A MN-major 64B swizzle over dk, B MN-major 128B swizzle over dv)
-                for (int kk = 0; kk < kC / 16; ++kk) {
-                    mma_ss(tmem + kColS, smem_desc(kbuf + (uint32_t)kk * 1024u, 8192, 512, kSwizzle64B),
-                           smem_desc(vbuf + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), id_kv, 1);
-                }
+                mma_group_kv(tmem + kColS, dkt, dvv, id_kv);
                 mma_commit(BAR(B_SFULL));        // after MMA2 as well: V tile c may take the next state copy
                 mma_commit(BAR(b_kvempty(s)));   // MMA1 and MMA4 were the readers of this K tile
                 if (save_images) {  // V(c+1) may land once the image store has read the copy
@@ -980,7 +1000,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             record_status(GLA_ERR_TIMEOUT);
             *abort_flag = 1;
         }
-    } else if (warp >= kEpiWarp0) {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------ epilogue warpgroup
         const int q4 = warp & 3;                            // TMEM lane quadrant of this warp
         const int r = 32 * q4 + lane;                       // TMEM lane = token row

@@ -47,6 +47,7 @@ SIGNATURES = {
     "gla_conv1d_silu_step": ([_P, _P, _P, _P, _P, _I, _I, _P], _I),
     "gla_last_device_status": ([_P], _I),
     "gla_status_str": ([_I], ctypes.c_char_p),
+    "gla_chunk_kernel": ([_I, _I, _I, _I, _I], _I),
     "gla_kernel_launches": ([], ctypes.c_uint64),
     "gla_version": ([], _I),
 }
@@ -439,6 +440,17 @@ def gla_last_device_status(stream=None) -> int:
 
 def gla_status_str(status: int) -> str:
     return load().gla_status_str(int(status)).decode()
+
+
+OP_FORWARD, OP_FORWARD_GATED, OP_BACKWARD = 0, 1, 2   # gla_op
+BF16, F32 = 0, 1                                      # gla_dtype
+KERNEL_TENSOR_CORE, KERNEL_SIMT = 1, 2                # gla_kernel_kind
+
+
+def gla_chunk_kernel(op: int, dtype: int, dk: int, dv: int, chunk: int) -> int:
+    """Which kernel a chunked entry point runs for these sizes on the current device: KERNEL_TENSOR_CORE,
+    KERNEL_SIMT, or a negative gla_status for sizes it rejects.  See include/gla.h."""
+    return int(load().gla_chunk_kernel(int(op), int(dtype), int(dk), int(dv), int(chunk)))
 
 
 def gla_kernel_launches() -> int:

@@ -92,11 +92,14 @@ typedef enum {
  *   B, T, H    batch, tokens per sequence, heads (all > 0)
  *   dk, dv     key / value head sizes: 16 <= dk <= 256 and 16 <= dv <= 512,
  *              both multiples of 8
- *   chunk      chunk length: 128 selects the tensor-core kernel (tcgen05/TMEM,
- *              fed by TMA) when 32 | dk <= 128 and 64 | dv <= 192 and its tiles fit
- *              in shared memory (every such shape but dk = 128 with dv = 192); 16, 32 or 64
- *              (and 128 outside that envelope) run the SIMT kernel, which
- *              splits a chunk that does not fit in shared memory in halves
+ *   chunk      chunk length 16, 32, 64 or 128: 128 and 64 select the
+ *              tensor-core kernel (tcgen05/TMEM, fed by TMA) when 32 | dk <= 128
+ *              and 64 | dv <= 192 and its tiles fit in shared memory (every
+ *              such shape but dk = 128 with dv = 192; chunk 64 as two chunks
+ *              per 128-row tile, see gla_chunk_kernel); 16 and 32, and any
+ *              chunk outside that envelope, run the SIMT kernel, which splits
+ *              a chunk that does not fit in shared memory in halves.
+ *              gla_chunk_kernel tells which kernel a call will run
  *   cu_seqlens NULL for a dense batch.  Otherwise a DEVICE int32 array [B+1]
  *              of packed sequence offsets: sequence s is rows
  *              cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed [1, T, ...]
@@ -435,6 +438,36 @@ GLA_API int gla_conv1d_silu_step(const void *x, const float *weight, const float
  * since the previous call.  Returns GLA_ERR_LAUNCH if synchronisation fails.
  */
 GLA_API int gla_last_device_status(void *stream);
+
+/*
+ * gla_chunk_kernel — which kernel a chunked entry point runs for these sizes on
+ * the current device (a host-side query; launches nothing).
+ *   op     GLA_OP_FORWARD (gla_chunk_fwd and its _noalloc, _host and _save
+ *          forms), GLA_OP_FORWARD_GATED (gla_chunk_fwd_gated) or GLA_OP_BACKWARD
+ *          (gla_chunk_bwd); else GLA_ERR_ARG
+ *   dtype  GLA_BF16 (the bf16 entry points) or GLA_F32 (the _f32 ones)
+ *   dk, dv, chunk  as the entry point would get them
+ * Returns GLA_KERNEL_TENSOR_CORE, GLA_KERNEL_SIMT, or a negative gla_status
+ * for sizes the entry point rejects (GLA_ERR_UNSUPPORTED, also on a device
+ * that is not sm_103).
+ *
+ * The tensor-core kernels (tcgen05 MMAs with TMEM accumulators, fed by TMA)
+ * take bf16 inputs with chunk 128 or 64, dk a multiple of 32 up to 128 and dv
+ * a multiple of 64 up to 192 whose tiles fit in shared memory: every such
+ * shape but dk 128 with dv 192, which needs 240 KB for the forward's two Q, K
+ * and V tiles against the 227 KB a block may use (the gated forward needs
+ * 16 KB more; the backward also needs dv + 2 dk <= 384).  A chunk of 64 runs
+ * as two 64-token chunks per 128-row tile: the second chunk's carried-state
+ * term through the first chunk's keys and values is the tile's lower-left
+ * attention block, which is the chunk-64 recurrence without rounding the
+ * state between the two chunks to bf16 (the same map up to rounding).  Every
+ * other case runs the f32-FMA SIMT kernel, which is correct for all of them
+ * but about ten times slower on the shapes both kernels take.
+ */
+typedef enum { GLA_OP_FORWARD = 0, GLA_OP_FORWARD_GATED = 1, GLA_OP_BACKWARD = 2 } gla_op;
+typedef enum { GLA_BF16 = 0, GLA_F32 = 1 } gla_dtype;
+typedef enum { GLA_KERNEL_TENSOR_CORE = 1, GLA_KERNEL_SIMT = 2 } gla_kernel_kind;
+GLA_API int gla_chunk_kernel(int op, int dtype, int dk, int dv, int chunk);
 
 /* gla_status_str — static, NUL-terminated description of a gla_status value. */
 GLA_API const char *gla_status_str(int status);

@@ -93,3 +93,12 @@ def test_host_entry_rejects_bad_arguments_before_any_copy(lib):
     assert lib.gla_chunk_fwd_host(fake, fake, fake, fake, None, fake, None, 1, 0, 1, 16, 16, 128, None) == -1
     assert lib.gla_chunk_fwd_host(fake, fake, fake, fake, None, fake, None, 1, 8, 1, 20, 64, 128, None) == -2
     assert lib.gla_chunk_fwd_host(fake, fake, fake, fake, None, fake, None, 1, 8, 1, 64, 64, 48, None) == -2
+
+
+def test_chunk_kernel_query_rejects_bad_arguments_on_the_host(lib):
+    # unknown operation or dtype, then sizes no entry point takes; on a host without an sm_103 device
+    # every valid query answers GLA_ERR_UNSUPPORTED
+    assert lib.gla_chunk_kernel(3, 0, 96, 192, 128) == -1
+    assert lib.gla_chunk_kernel(0, 2, 96, 192, 128) == -1
+    assert lib.gla_chunk_kernel(0, 0, 20, 192, 128) == -2
+    assert lib.gla_chunk_kernel(2, 0, 96, 192, 48) == -2

@@ -123,6 +123,34 @@ def test_bf16_direct_decay_form_head_sizes(dk, dv):
     assert oracle.rel_err(hT.cpu().numpy(), h_ref) <= 1e-2
 
 
+def test_chunk_kernel_query_and_chunk64_on_tensor_cores():
+    """gla_chunk_kernel names the kernel a call runs; chunk 64 runs on the tensor cores (two chunks per
+    128-row tile) and gives exactly the chunk-128 result, forward and backward."""
+    TC, SIMT = gla.KERNEL_TENSOR_CORE, gla.KERNEL_SIMT
+    for op in (gla.OP_FORWARD, gla.OP_FORWARD_GATED, gla.OP_BACKWARD):
+        assert gla.gla_chunk_kernel(op, gla.BF16, 96, 192, 128) == TC
+        assert gla.gla_chunk_kernel(op, gla.BF16, 96, 192, 64) == TC
+        assert gla.gla_chunk_kernel(op, gla.BF16, 96, 192, 32) == SIMT
+        assert gla.gla_chunk_kernel(op, gla.F32, 96, 192, 128) == SIMT
+        assert gla.gla_chunk_kernel(op, gla.BF16, 48, 80, 128) == SIMT
+        assert gla.gla_chunk_kernel(op, gla.BF16, 128, 192, 128) == SIMT  # 240 KB of tiles
+        assert gla.gla_chunk_kernel(op, gla.BF16, 96, 192, 100) == -2
+    assert gla.gla_chunk_kernel(gla.OP_BACKWARD, gla.BF16, 32, 256, 128) == SIMT
+    assert gla.gla_chunk_kernel(7, gla.BF16, 96, 192, 128) == -1
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=300, H=3, h0_std=0.02)
+    d = with_dev_cu(I.make_backward(w, device="cuda", seed=17))
+    o64, h64 = run_prefill(d, 64)
+    o128, h128 = run_prefill(d, 128)
+    assert torch.equal(o64, o128) and torch.equal(h64, h128)
+    g64 = gla.chunk_bwd(d["q"], d["k"], d["v"], d["dout"], d["log_decay"], d["h0"], d["dhT"], chunk=64)
+    g128 = gla.chunk_bwd(d["q"], d["k"], d["v"], d["dout"], d["log_decay"], d["h0"], d["dhT"], chunk=128)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(g64, g128))
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(o64.float().cpu().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(h64.cpu().numpy(), h_ref) <= 1e-2
+
+
 @pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 256, 385])
 def test_bf16_lengths(T):
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=T, H=2, h0_std=0.05)

@@ -113,10 +113,19 @@ def test_forward_save_and_saved_backward(name):
 
 
 def test_shapes_outside_the_tensor_core_backward_are_refused():
+    """Saved states exist only on the tensor-core kernels: chunk 32 (SIMT) is refused, chunk 64 runs as two
+    chunks per 128-row tile and gives exactly the chunk-128 result."""
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=64, H=2, dk=96, dv=192)
     d = I.make_prefill(w, device="cuda", seed=1)
     out = torch.empty(1, 64, 2, 192, dtype=torch.bfloat16, device="cuda")
     img = gla.state_images(d["q"], d["v"])
     with pytest.raises(gla.GLAError) as e:
-        gla.gla_chunk_fwd_save(d["q"], d["k"], d["v"], d["log_decay"], None, out, None, img, 64)
-    assert e.value.status == -2  # GLA_ERR_UNSUPPORTED: chunk 64 runs on the SIMT kernels
+        gla.gla_chunk_fwd_save(d["q"], d["k"], d["v"], d["log_decay"], None, out, None, img, 32)
+    assert e.value.status == -2  # GLA_ERR_UNSUPPORTED: chunk 32 runs on the SIMT kernels
+    out128 = torch.empty_like(out)
+    img.zero_()  # slots no chunk starts at are left untouched by both calls
+    img128 = torch.zeros_like(img)
+    gla.gla_chunk_fwd_save(d["q"], d["k"], d["v"], d["log_decay"], None, out, None, img, 64)
+    gla.gla_chunk_fwd_save(d["q"], d["k"], d["v"], d["log_decay"], None, out128, None, img128, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out128) and torch.equal(img, img128)

@@ -116,3 +116,34 @@ def test_layer_range_is_checked():
     out = torch.empty(2, 4, 4, 192, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(gla.GLAError):
         gla.gla_decode_step_layers(q, k, v, ld, pool, slots, out, layer0=1)  # layers 1, 2 of 2-layer pages
+
+
+def test_layers_bench_configuration_sampled_layers():
+    """The bench's multi-layer leg: 128 sequences whose pages hold all 24 layers (H16, 96 x 192), one launch
+    for every layer; three layers of every sequence are checked against the reference step, and the whole
+    pool against one call per layer (bit for bit)."""
+    L, N, H = 24, 128, 16
+    gen = torch.Generator().manual_seed(13)
+    s = 1.0 / np.sqrt(96)
+    q = (torch.randn(L, N, H, 96, generator=gen) * s).to(torch.bfloat16).cuda()
+    k = (torch.randn(L, N, H, 96, generator=gen) * s).to(torch.bfloat16).cuda()
+    v = torch.randn(L, N, H, 192, generator=gen).to(torch.bfloat16).cuda()
+    ld = torch.stack([I.log_decays(H)] * L).cuda()
+    pool = (torch.randn(N, L, H, 96, 192, generator=gen) * 0.02).cuda()
+    slots = torch.randperm(N, generator=gen).to(torch.int32).cuda()
+    pool_b = pool.clone()
+    out = torch.empty(L, N, H, 192, dtype=torch.bfloat16, device="cuda")
+    out_b = torch.empty_like(out)
+    sampled = (0, 11, 23)
+    pages0 = {l: pool[slots.long(), l].cpu() for l in sampled}
+    gla.gla_decode_step_layers(q, k, v, ld, pool, slots, out)
+    for l in range(L):
+        gla.gla_decode_step_layers(q[l:l + 1].contiguous(), k[l:l + 1].contiguous(), v[l:l + 1].contiguous(),
+                                   ld[l:l + 1].contiguous(), pool_b, slots, out_b[l:l + 1], layer0=l)
+    torch.cuda.synchronize()
+    assert gla.gla_last_device_status() == 0
+    assert torch.equal(out, out_b) and torch.equal(pool, pool_b)
+    for l in sampled:
+        o_ref, s_ref = oracle.decode_step(q[l], k[l], v[l], ld[l], pages0[l])
+        assert oracle.rel_err(out[l].float().cpu().numpy(), o_ref) <= TOL
+        assert oracle.rel_err(pool[slots.long(), l].cpu().numpy(), s_ref) <= 1e-5

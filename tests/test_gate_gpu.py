@@ -148,3 +148,10 @@ def test_gate_arguments_are_checked():
                                         d["log_decay"].data_ptr(), None, out.data_ptr(), None, 1, 128, 2, w.dk,
                                         w.dv, 128, None, None)
     assert rc == -1  # GLA_ERR_ARG: no gate
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_gated_prefill_layer_workload_full_size(kind):
+    """The bench's gated leg at full size (B8 T2048 H16 dk96 dv192, g ~ N(0, 2^2)): every chain's gated
+    output and final state against the reference."""
+    check_gated_prefill(I.WORKLOADS["layer_bf16"], kind, seed=0)

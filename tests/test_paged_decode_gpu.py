@@ -123,3 +123,20 @@ def test_slot_beyond_pool_is_reported_and_skipped():
     named = set(slots.cpu().tolist()) - {16}
     others = [i for i in range(16) if i not in named]
     assert torch.equal(pool[others], pool0[others])
+
+
+def test_paged_decode_workload_full_size():
+    """The bench's paged leg: N1280 x H16 states 96 x 192 as a pool read through a seeded permutation of the
+    pages; every output and every page against the reference step."""
+    w = I.WORKLOADS["decode"]
+    d = I.make_decode(w, device="cuda", seed=0)
+    pool = d["state"]
+    slots = torch.randperm(w.B, generator=torch.Generator().manual_seed(7)).to(torch.int32).cuda()
+    pool0 = pool.cpu().numpy().astype(np.float64)
+    out = torch.empty_like(d["v"])
+    gla.gla_decode_step_paged(d["q"], d["k"], d["v"], d["log_decay"], pool, slots, out)
+    torch.cuda.synchronize()
+    o_ref, pool_ref = reference(d, pool0, slots)
+    assert oracle.rel_err(out.float().cpu().numpy(), o_ref) <= TOL
+    assert oracle.rel_err(pool.cpu().numpy(), pool_ref) <= 1e-5
+    assert gla.gla_last_device_status() == 0

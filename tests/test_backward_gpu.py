@@ -130,3 +130,32 @@ def test_backward_segmented_state_passes(T, H, lo, hi):
     chunk, the last case mixes heads the SIMT recurrences own."""
     w = I.scaled(I.WORKLOADS["long_bf16"], B=1, T=T, H=H, h0_std=0.02, decay_lo=lo, decay_hi=hi)
     check_backward(w, seed=T)
+
+
+def rel_err_rows(got, ref, rows=4096):
+    """max|got - ref| / max|ref| over a full-size gradient, in blocks of the token axis."""
+    num = den = 0.0
+    for a in range(0, ref.shape[1], rows):
+        g = got[:, a:a + rows].float().cpu().numpy().astype(np.float64)
+        r = ref[:, a:a + rows]
+        num = max(num, float(np.max(np.abs(g - r))))
+        den = max(den, float(np.max(np.abs(r))))
+    return num / den if den else num
+
+
+@pytest.mark.parametrize("name", ["long_bf16", "ragged"])
+def test_backward_long_and_ragged_workloads_full_size(name):
+    """The backward at the long-context size (B1 T32768 H16 with h0 and dhT: both state passes segmented) and
+    at the ragged packed batch (64 sequences of U[1, 8192] tokens): every chain's dq, dk, dv and dh0."""
+    w = I.WORKLOADS[name]
+    d = I.make_backward(w, device="cuda", seed=2, dhT_std=0.02)
+    cu = None if d["cu_seqlens"] is None else d["cu_seqlens"].cuda()
+    grads = gla.chunk_bwd(d["q"], d["k"], d["v"], d["dout"], d["log_decay"], d["h0"], d["dhT"], chunk=128,
+                          cu_seqlens=cu)
+    torch.cuda.synchronize()
+    assert gla.gla_last_device_status() == 0
+    ref = oracle.backward(d["q"], d["k"], d["v"], d["dout"], d["log_decay"], d["h0"], d["dhT"],
+                          cu_seqlens=d["cu_seqlens"])
+    errs = {n: rel_err_rows(g, r) for n, g, r in zip(NAMES[:3], grads[:3], ref[:3])}
+    errs["dh0"] = oracle.rel_err(grads[3].cpu().numpy(), ref[3])
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs

@@ -33,7 +33,8 @@
 //   MMA4   dK  = P2 Q + V G_c^T   -> [dv, dv+dk)
 //   MMA5   B   = dO V^T           -> scratch              mask -> P3
 //   MMA6   dQ  = P3 K + dO S^T    -> [dv+dk, dv+2dk)
-//   epilogue: row factors, bf16, stores of the rows below L.
+//   epilogue: row factors, bf16, stores of the rows below L; in a full chunk dV and dK
+//          are staged over V and Q and stored while mask 3 and MMA6 run, dQ after MMA6.
 #include <mutex>
 
 #include "gla_common.cuh"
@@ -147,11 +148,12 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
     tmem_wait_st();
 }
 
-// Row r of an accumulator of `ncols` columns at tcol, times f, as bf16 into a staging tile laid out as
-// the TMA box of the output: 64-column atoms of 128-byte rows with the 128B swizzle (atom_cols 64), or
-// 32-column atoms of 64-byte rows with the 64B swizzle (atom_cols 32).
-__device__ __forceinline__ void stage_row(uint32_t tcol, int ncols, float f, int r, uint8_t *tile, int atom_cols) {
-    for (int c0 = 0; c0 < ncols; c0 += 32) {
+// Columns [c_begin, c_end) (multiples of 32) of row r of an accumulator at tcol, times f, as bf16 into a
+// staging tile laid out as the TMA box of the output: 64-column atoms of 128-byte rows with the 128B
+// swizzle (atom_cols 64), or 32-column atoms of 64-byte rows with the 64B swizzle (atom_cols 32).
+__device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end, float f, int r, uint8_t *tile,
+                                          int atom_cols) {
+    for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         uint32_t a[32];
         tmem_ld32(tcol + (uint32_t)c0, a);
         tmem_wait_ld();
@@ -385,7 +387,10 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
     }
     // P3 = B_ij kept for j <= i, times lambda^-(j+1)
-    wait_mma();
+    wait_mma();  // MMA4, MMA5 done: dV and dK are final, and no MMA reads Q, V or G any more
+    // A full chunk stages dV (over V) and dK (over Q) and starts their stores while mask 3 and MMA6 run,
+    // so that only dQ is left once MMA6 is done.  One decision for the whole CTA (it has barriers).
+    const bool early = __syncthreads_and(ok && L == kC) != 0;
     masked(true, utab);
     if (tid == 0) {
         wait_mask();
@@ -398,34 +403,44 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mma_commit(BAR(B_MMA));
         }
     }
+    const float rf = tab[max(L - 1 - r, 0)];  // lambda^(L-1-j) for dV and dK
+    const float qf = tab[min(r + 1, kC)];     // lambda^(i+1) for dQ
+    if (early) {
+        // the two halves of the warps split the dv + dk columns: dV's first columns to one, the rest of dV
+        // and dK to the other
+        const int vsplit = min(dv, 32 * ((dv + dk) / 64));
+        if (half == 0) {
+            stage_row(tmem + lane_base + colDV, 0, vsplit, rf, r, smem + plan.v, 64);
+        } else {
+            stage_row(tmem + lane_base + colDV, vsplit, dv, rf, r, smem + plan.v, 64);
+            stage_row(tmem + lane_base + colDK, 0, dk, rf, r, smem + plan.q, 32);
+        }
+        fence_async_shared();
+        named_bar_sync(2, kThreads);
+        if (tid == 0) {
+            const int y = (int)row0;
+            for (int a = 0; a < nva; ++a) tma_store_2d(&tmDV, h * dv + 64 * a, y, vb + a * 16384u);
+            for (int a = 0; a < nka; ++a) tma_store_2d(&tmDK, h * dk + 32 * a, y, qb + a * 8192u);
+            bulk_commit();
+        }
+    }
     wait_mma();
 
-    // ---- epilogue: row factors, bf16, rows below L ----
+    // ---- epilogue: dQ (and for a partial chunk everything): row factors, bf16, rows below L ----
     ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA: the epilogue has a barrier
     if (ok) {
-        const float rf = tab[max(L - 1 - r, 0)];  // lambda^(L-1-j) for dV and dK
-        const float qf = tab[min(r + 1, kC)];     // lambda^(i+1) for dQ
-        // the first half of the warps takes dV (dv columns), the second dK and dQ (2 dk columns)
         if (L == kC) {
-            // a full chunk: every tile is free now; stage the rows as TMA boxes (dV over V, dK over K,
-            // dQ over Q) and write them with one store per atom
-            if (half == 0) {
-                stage_row(tmem + lane_base + colDV, dv, rf, r, smem + plan.v, 64);
-            } else {
-                stage_row(tmem + lane_base + colDK, dk, rf, r, smem + plan.k, 32);
-                stage_row(tmem + lane_base + colDQ, dk, qf, r, smem + plan.q, 32);
-            }
+            // a full chunk (so `early` held): dQ staged over K, which MMA6 was the last to read, its 32-column
+            // atoms split between the halves, and written with one store per atom
+            const int qsplit = 32 * ((nka + 1) / 2);
+            stage_row(tmem + lane_base + colDQ, half == 0 ? 0 : qsplit, half == 0 ? qsplit : dk, qf, r,
+                      smem + plan.k, 32);
             fence_async_shared();
-            __syncthreads();
+            named_bar_sync(2, kThreads);
             if (tid == 0) {
                 const int y = (int)row0;
-                for (int a = 0; a < nva; ++a) tma_store_2d(&tmDV, h * dv + 64 * a, y, vb + a * 16384u);
-                for (int a = 0; a < nka; ++a) {
-                    tma_store_2d(&tmDK, h * dk + 32 * a, y, kb + a * 8192u);
-                    tma_store_2d(&tmDQ, h * dk + 32 * a, y, qb + a * 8192u);
-                }
+                for (int a = 0; a < nka; ++a) tma_store_2d(&tmDQ, h * dk + 32 * a, y, kb + a * 8192u);
                 bulk_commit();
-                bulk_wait_read0();  // the stores must have read shared memory before the CTA exits
             }
         } else {
             // the last chunk of a sequence: rows from L on belong to the next one; plain stores
@@ -441,6 +456,9 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     } else if (tid == 0) {
         record_status(GLA_ERR_TIMEOUT);
     }
+    // the stores must have read shared memory before the CTA exits (also those of dV and dK when a later
+    // wait gave up)
+    if (tid == 0 && early) bulk_wait_read0();
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();

@@ -178,14 +178,17 @@ GLA_API int gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v, c
  *
  * Computes the map of gla_chunk_fwd (same recurrence, same kernels) for a
  * dense batch whose q, k, v, log_decay and h0 live in host memory, and writes
- * out and hT to host memory.  The batch is cut into groups of whole sequences
- * (at most 8 groups, none under 8 MiB of copies unless the batch is smaller);
- * group g+1 is copied to the device while group g computes on `stream` and
- * group g-1 is copied back on a third (the library's own), so the copies in
- * both directions and the compute run at the same time.  A group's
- * sequences are computed as a batch of their own, so results can differ from
- * one gla_chunk_fwd call on the whole batch in the last bits (the schedule
- * depends on the number of chains), never by more than rounding.
+ * out and hT to host memory.  The work is cut into at most 8 groups, none
+ * under 8 MiB of copies unless the batch is smaller: groups of whole
+ * sequences, or, when that makes more groups (few, long sequences), ranges of
+ * whole chunks of rows of every sequence, each computed from the state the
+ * previous range left.  Group g+1 is copied to the device while group g
+ * computes on `stream` and group g-1 is copied back on a third (the
+ * library's own), so the copies in both directions and the compute run at the
+ * same time.  A group is computed as a gla_chunk_fwd call of its own, so
+ * results can differ from one gla_chunk_fwd call on the whole batch in the
+ * last bits (the schedule depends on the number of chains and chunks), never
+ * by more than rounding.
  *
  * Arguments are those of gla_chunk_fwd without cu_seqlens (packed batches are
  * not taken here), with every array a HOST pointer in the same layout:

@@ -1,10 +1,12 @@
 """GPU parity of gla_chunk_fwd_host: the chunked forward on host arrays, copies overlapped by groups.
 
-The entry point cuts the batch into groups of whole sequences and runs copy-in, compute and copy-out
-of consecutive groups on three streams.  Checks: results against the fp64 reference (same 1e-2 bar
-as the device entry point), bit-identity with the device entry point called on the same group
-(the kernels are deterministic and a group is computed as a batch of its own), pageable host memory,
-missing h0 / hT, and the full layer workload (eight groups) sampled against the reference.
+The entry point cuts the work into groups (of whole sequences, or, for few long sequences, ranges of
+whole chunks of rows of every sequence, each started from the state the previous range left) and runs
+copy-in, compute and copy-out of consecutive groups on three streams.  Checks: results against the
+fp64 reference (same 1e-2 bar as the device entry point), bit-identity with the device entry point
+called on the same groups (the kernels are deterministic and a group is computed as a call of its
+own), pageable host memory, missing h0 / hT, the full layer workload (eight groups of one sequence)
+and the full long-context workload (eight time ranges).
 """
 import numpy as np
 import pytest
@@ -43,6 +45,39 @@ def host_forward(d, chunk, pinned=True, with_h0=True, with_hT=True):
     s.synchronize()
     assert gla.gla_last_device_status() == 0
     return out, hT
+
+
+def host_groups(B, T, H, dk, dv, chunk, with_h0=True, with_hT=True):
+    """How gla_chunk_fwd_host cuts the work, by the rule its header states: at most 8 groups, none under
+    8 MiB of copies unless the batch is smaller; whole sequences, or ranges of whole chunks when those
+    make more groups.  Returns ("sequences", sequences per group) or ("ranges", rows per range)."""
+    max_groups, min_bytes = 8, 8 << 20
+    cdiv = lambda a, b: -(-a // b)
+    seq_b = T * H * (2 * dk + 2 * dv) * 2 + (int(with_h0) + int(with_hT)) * H * dk * dv * 4
+    per_group = cdiv(B, max_groups)
+    if per_group < cdiv(min_bytes, seq_b):
+        per_group = min(cdiv(min_bytes, seq_b), B)
+    ngroups = cdiv(B, per_group)
+    nch = cdiv(T, chunk)
+    chunk_b = B * chunk * H * (2 * dk + 2 * dv) * 2
+    per = cdiv(nch, max_groups)
+    if per < cdiv(min_bytes, chunk_b):
+        per = min(cdiv(min_bytes, chunk_b), nch)
+    return ("ranges", per * chunk) if cdiv(nch, per) > ngroups else ("sequences", per_group)
+
+
+def chained_device_forward(d, chunk, rows):
+    """The device entry point over consecutive ranges of `rows` rows of every sequence, each range started
+    from the state the previous one left."""
+    T = d["q"].shape[1]
+    h, outs = d["h0"], []
+    for t0 in range(0, T, rows):
+        sl = slice(t0, t0 + rows)
+        o, h = gla.chunk_fwd(d["q"][:, sl].contiguous(), d["k"][:, sl].contiguous(), d["v"][:, sl].contiguous(),
+                             d["log_decay"], h, chunk=chunk)
+        outs.append(o)
+    torch.cuda.synchronize()
+    return torch.cat(outs, dim=1).cpu(), h.cpu()
 
 
 def device_forward(d, chunk, b0=0, b1=None, with_h0=True):
@@ -96,3 +131,43 @@ def test_host_forward_rejects_device_tensors():
     out = torch.empty(1, 64, 2, w.dv, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         gla.gla_chunk_fwd_host(d["q"], d["k"], d["v"], d["log_decay"], None, out, None, 128)
+
+
+@pytest.mark.parametrize("B_", [1, 2])
+def test_host_forward_time_ranges_match_chained_device_calls(B_):
+    """Few long sequences (T = 64 chunks + 100 rows): the work is cut in time.  The result must equal the
+    device entry point called range by range with the state carried over, bit for bit, and the
+    reference within the bar."""
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=B_, T=64 * 128 + 100, H=4, h0_std=0.02)
+    kind, rows = host_groups(B_, w.T, w.H, w.dk, w.dv, 128)
+    assert kind == "ranges" and rows % 128 == 0 and rows < w.T, (kind, rows)
+    d = I.make_prefill(w, device="cuda", seed=11)
+    out, hT = host_forward(d, 128)
+    oc, hc = chained_device_forward(d, 128, rows)
+    assert torch.equal(out, oc) and torch.equal(hT, hc)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(out.float().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.numpy(), h_ref) <= 1e-2
+
+
+def test_host_forward_time_ranges_pageable_memory_and_no_states():
+    w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=4000, H=2)
+    assert host_groups(1, w.T, w.H, w.dk, w.dv, 128, False, False)[0] == "ranges"
+    d = I.make_prefill(w, device="cuda", seed=12)
+    out, _ = host_forward(d, 128, pinned=False, with_h0=False, with_hT=False)
+    o_ref, _ = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], None)
+    assert oracle.rel_err(out.float().numpy(), o_ref) <= 1e-2
+
+
+def test_host_forward_long_workload_eight_time_ranges():
+    """B1 T32768 H16 with h0: eight ranges of 4,096 rows, every chain against the reference, and the
+    result equal to the chained device calls bit for bit."""
+    w = I.WORKLOADS["long_bf16"]
+    assert host_groups(w.B, w.T, w.H, w.dk, w.dv, 128) == ("ranges", 4096)
+    d = I.make_prefill(w, device="cuda", seed=13)
+    out, hT = host_forward(d, 128)
+    oc, hc = chained_device_forward(d, 128, 4096)
+    assert torch.equal(out, oc) and torch.equal(hT, hc)
+    o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
+    assert oracle.rel_err(out.float().numpy(), o_ref) <= 1e-2
+    assert oracle.rel_err(hT.numpy(), h_ref) <= 1e-2

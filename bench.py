@@ -466,6 +466,36 @@ def run_prefill_workload(args, name, stream, peaks, peak_src, dev, seed):
     by = rows * w.H * 2 * (2 * w.dk + 2 * w.dv) + (st_bytes if d["h0"] is not None else 0) + st_bytes
     fl = prefill_flops(1, rows, w.H, w.dk, w.dv, w.chunk)
     gbs = by / (us / 1e6) / 1e9
+    e2e = None
+    if cu is None:
+        # the same forward through the public API on pinned host arrays (gla_chunk_fwd_host; few long
+        # sequences are cut into chunk-aligned time ranges so that copies and compute overlap)
+        host = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "log_decay")}
+        h_h0 = None if d["h0"] is None else d["h0"].cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_hT = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+
+        def host_step():
+            gla.gla_chunk_fwd_host(host["q"], host["k"], host["v"], host["log_decay"], h_h0, h_out, h_hT, w.chunk,
+                                   stream)
+
+        for _ in range(2):
+            host_step()
+        torch.cuda.synchronize()
+        ne = max(3, min(args.steps, 8))
+        eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(ne)]
+        for e in eve:
+            e[0].record(stream)
+            host_step()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(e[0].elapsed_time(e[1]) for e in eve)
+        h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + [h_h0] if t is not None)
+        d2h = h_out.numel() * h_out.element_size() + h_hT.numel() * h_hT.element_size()
+        e2e = {"value": rows / (ms / 1e3), "unit": "tokens/s", "ms": ms, "steps": ne, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "copy_gbs": (h2d + d2h) / (ms / 1e3) / 1e9,
+               "note": "gla_chunk_fwd_host on pinned host arrays in and out, CUDA events around each call (median)"}
+        del host, h_h0, h_out, h_hT
     return {"value": rows / (us / 1e6), "unit": "tokens/s", "us": us, "us_median": statistics.median(times) * 1e3,
             "us_best": min(times) * 1e3, "steps": n, "launches_per_call": launches, "tokens": rows, "sequences": nseq,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -475,7 +505,7 @@ def run_prefill_workload(args, name, stream, peaks, peak_src, dev, seed):
                                                      f"prefill_{name}"),
                          "tensor": {"achieved_tflops": fl / (us / 1e6) / 1e12, "peak_tflops": peaks["bf16_tflops"],
                                     "frac": fl / (us / 1e6) / 1e12 / peaks["bf16_tflops"], "flops_per_launch": fl}},
-            "workload": w.note, "kernel": f"gla_chunk_fwd ({name})"}
+            "workload": w.note, "kernel": f"gla_chunk_fwd ({name})", "e2e": e2e}
 
 
 def run_paged_decode(args, D, wd, dout, stream, peaks):

@@ -133,17 +133,17 @@ def test_host_forward_rejects_device_tensors():
         gla.gla_chunk_fwd_host(d["q"], d["k"], d["v"], d["log_decay"], None, out, None, 128)
 
 
-@pytest.mark.parametrize("B_", [1, 2])
-def test_host_forward_time_ranges_match_chained_device_calls(B_):
-    """Few long sequences (T = 64 chunks + 100 rows): the work is cut in time.  The result must equal the
-    device entry point called range by range with the state carried over, bit for bit, and the
-    reference within the bar."""
+@pytest.mark.parametrize("B_,chunk", [(1, 128), (2, 128), (1, 64), (1, 32)])
+def test_host_forward_time_ranges_match_chained_device_calls(B_, chunk):
+    """Few long sequences (T = 64 chunks of 128 + 100 rows): the work is cut in time, in whole chunks.  The
+    result must equal the device entry point called range by range with the state carried over, bit for
+    bit, and the reference within the bar (chunk 32 runs the SIMT kernel, the others the tensor cores)."""
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=B_, T=64 * 128 + 100, H=4, h0_std=0.02)
-    kind, rows = host_groups(B_, w.T, w.H, w.dk, w.dv, 128)
-    assert kind == "ranges" and rows % 128 == 0 and rows < w.T, (kind, rows)
+    kind, rows = host_groups(B_, w.T, w.H, w.dk, w.dv, chunk)
+    assert kind == "ranges" and rows % chunk == 0 and rows < w.T, (kind, rows)
     d = I.make_prefill(w, device="cuda", seed=11)
-    out, hT = host_forward(d, 128)
-    oc, hc = chained_device_forward(d, 128, rows)
+    out, hT = host_forward(d, chunk)
+    oc, hc = chained_device_forward(d, chunk, rows)
     assert torch.equal(out, oc) and torch.equal(hT, hc)
     o_ref, h_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["log_decay"], d["h0"])
     assert oracle.rel_err(out.float().numpy(), o_ref) <= 1e-2

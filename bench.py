@@ -361,6 +361,7 @@ def run_ours(args, world, rank, local):
     # ---- the other prefill workloads: long context (segmented schedule) and the ragged packed batch ----
     long_leg = run_prefill_workload(args, "long_bf16", stream, peaks, peak_src, dev, rank)
     ragged_leg = run_prefill_workload(args, "ragged", stream, peaks, peak_src, dev, rank)
+    tiny_leg = run_tiny_f32(args, stream, dev, rank)
 
     # ---- end to end through the public API: pinned host inputs in, results back to the host ----
     e2e = run_e2e(args, P, D, w, wd, out, hT, dout, stream)
@@ -406,6 +407,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "prefill_long": long_leg,
         "prefill_ragged": ragged_leg,
+        "prefill_tiny_f32": tiny_leg,
         "decode_paged": paged,
         "prefill_gated": gated,
         "decode_layers": layers,
@@ -506,6 +508,41 @@ def run_prefill_workload(args, name, stream, peaks, peak_src, dev, seed):
                          "tensor": {"achieved_tflops": fl / (us / 1e6) / 1e12, "peak_tflops": peaks["bf16_tflops"],
                                     "frac": fl / (us / 1e6) / 1e12 / peaks["bf16_tflops"], "flops_per_launch": fl}},
             "workload": w.note, "kernel": f"gla_chunk_fwd ({name})", "e2e": e2e}
+
+
+def run_tiny_f32(args, stream, dev, seed):
+    """gla_chunk_fwd_f32 on the small fp32 parity workload (B1 H2 T256 dk=dv=64, chunk 64): CUDA events
+    around each of up to 30 back-to-back calls (median).  A latency number, not a roofline one: two chains
+    of four chunks occupy two SMs for a few microseconds."""
+    import torch
+    from gated_linear_rnn_gb300 import gla
+    from gated_linear_rnn_gb300 import inputs as I
+    w = I.WORKLOADS["tiny_f32"]
+    d = I.make_prefill(w, device=dev, seed=seed)
+    out = torch.empty(d["q"].shape[:3] + (w.dv,), dtype=torch.float32, device=dev)
+    hT = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+
+    def step():
+        gla.gla_chunk_fwd_f32(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, hT, w.chunk, None, stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(5, min(args.steps, 30))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for e in ev:
+        e[0].record(stream)
+        step()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    st_code = gla.gla_last_device_status(stream)
+    if st_code != 0:
+        raise SystemExit(f"device status after the tiny f32 prefill: {st_code} ({gla.gla_status_str(st_code)})")
+    us = statistics.median(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    kind = gla.gla_chunk_kernel(gla.OP_FORWARD, gla.F32, w.dk, w.dv, w.chunk)
+    return {"value": w.B * w.T / (us / 1e6), "unit": "tokens/s", "us": us, "steps": n,
+            "kernel": "tensor cores" if kind == gla.KERNEL_TENSOR_CORE else "SIMT",
+            "workload": w.note, "note": "the parity configuration; latency-bound, reported for completeness"}
 
 
 def run_paged_decode(args, D, wd, dout, stream, peaks):

@@ -119,10 +119,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&p)[16
 // is multiplied by colf[x].  The two warps of a lane quadrant take score columns [64 half, 64 half + 64)
 // each; P block b (16 columns) overwrites score block b / 2, which the other half may still read, so
 // every thread holds its scores in registers before the CTA barrier and writes P after it.  The barrier
-// is reached by every thread (also when `live` is false: then the warp only passes it).
+// is reached by every thread (also when `live` is false: then the warp only passes it).  The kept
+// columns of each 32-column block are one 32-bit mask (bit t for column 32 b + t), so no per-element
+// comparison is kept live.
 __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool lower, const float *colf, int half,
                                             bool live) {
-    const bool row_ok = r < L;
     uint32_t a[2][32];
     if (live) {
         tmem_ld32(tbase + (uint32_t)(64 * half), a[0]);
@@ -134,14 +135,17 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
 #pragma unroll
     for (int bb = 0; bb < 2; ++bb) {
         const int b = 2 * half + bb;
+        const int d = r - 32 * b, lim = L - 32 * b;
+        uint32_t bits = lower ? (d >= 31 ? 0xffffffffu : d < 0 ? 0u : (2u << d) - 1u)
+                              : (d <= 0 ? 0xffffffffu : d > 31 ? 0u : ~((1u << d) - 1u));
+        bits &= lim >= 32 ? 0xffffffffu : lim <= 0 ? 0u : (1u << lim) - 1u;
+        if (r >= L) bits = 0u;
         uint32_t p[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int x0 = 32 * b + 2 * e, x1 = x0 + 1;
-            const bool k0 = row_ok && x0 < L && (lower ? x0 <= r : x0 >= r);
-            const bool k1 = row_ok && x1 < L && (lower ? x1 <= r : x1 >= r);
-            p[e] = pack_bf16x2(k0 ? __uint_as_float(a[bb][2 * e]) * colf[x0] : 0.f,
-                               k1 ? __uint_as_float(a[bb][2 * e + 1]) * colf[x1] : 0.f);
+            p[e] = pack_bf16x2(((bits >> (2 * e)) & 1u) ? __uint_as_float(a[bb][2 * e]) * colf[x0] : 0.f,
+                               ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(a[bb][2 * e + 1]) * colf[x1] : 0.f);
         }
         tmem_st16(tbase + (uint32_t)(16 * b), p);
     }

@@ -958,12 +958,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tmem_ld32(tmem + lane_base + kColA + (uint32_t)(32 * b), a);
                     tmem_wait_ld();
                     if (fact) {
-                        // the decay already sits in K'' and in the epilogue's row factor: causal mask only
+                        // the decay already sits in K'' and in the epilogue's row factor: causal mask only,
+                        // as one 32-bit mask of the block's kept columns (bit t for column 32 b + t)
+                        const int d = r - 32 * b;
+                        const uint32_t bits = !row_ok ? 0u : d >= 31 ? 0xffffffffu : d < 0 ? 0u : (2u << d) - 1u;
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const int j = 32 * b + 2 * e;
-                            const float x0 = (row_ok && j <= r) ? __uint_as_float(a[2 * e]) : 0.f;
-                            const float x1 = (row_ok && j + 1 <= r) ? __uint_as_float(a[2 * e + 1]) : 0.f;
+                            const float x0 = ((bits >> (2 * e)) & 1u) ? __uint_as_float(a[2 * e]) : 0.f;
+                            const float x1 = ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(a[2 * e + 1]) : 0.f;
                             p[e] = pack_bf16x2(x0, x1);
                         }
                     } else {

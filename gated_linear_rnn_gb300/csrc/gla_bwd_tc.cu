@@ -141,11 +141,15 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
         bits &= lim >= 32 ? 0xffffffffu : lim <= 0 ? 0u : (1u << lim) - 1u;
         if (r >= L) bits = 0u;
         uint32_t p[16];
+        const float4 *cf4 = reinterpret_cast<const float4 *>(colf + 32 * b);  // 16-byte aligned table
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int x0 = 32 * b + 2 * e, x1 = x0 + 1;
-            p[e] = pack_bf16x2(((bits >> (2 * e)) & 1u) ? __uint_as_float(a[bb][2 * e]) * colf[x0] : 0.f,
-                               ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(a[bb][2 * e + 1]) * colf[x1] : 0.f);
+        for (int g = 0; g < 8; ++g) {
+            const float4 c4 = cf4[g];
+            const int e = 2 * g;
+            p[e] = pack_bf16x2(((bits >> (2 * e)) & 1u) ? __uint_as_float(a[bb][2 * e]) * c4.x : 0.f,
+                               ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(a[bb][2 * e + 1]) * c4.y : 0.f);
+            p[e + 1] = pack_bf16x2(((bits >> (2 * e + 2)) & 1u) ? __uint_as_float(a[bb][2 * e + 2]) * c4.z : 0.f,
+                                   ((bits >> (2 * e + 3)) & 1u) ? __uint_as_float(a[bb][2 * e + 3]) * c4.w : 0.f);
         }
         tmem_st16(tbase + (uint32_t)(16 * b), p);
     }

@@ -282,7 +282,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // the 1024-aligned base, by pointer arithmetic on the shared array (not through an integer), so that
+    // every access derived from it compiles to a shared-memory instruction
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int dk = P.dk, dv = P.dv, H = P.H;
     const int nka = dk / 32, nva = dv / 64;
     // shared-memory offsets (scalars: nothing of the plan lives in local memory)

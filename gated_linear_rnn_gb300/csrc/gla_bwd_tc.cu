@@ -122,7 +122,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&p)[16
 // is reached by every thread (also when `live` is false: then the warp only passes it).  The kept
 // columns of each 32-column block are one 32-bit mask (bit t for column 32 b + t), so no per-element
 // comparison is kept live.
-__device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool lower, const float *colf, int half,
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool lower, uint32_t colf, int half,
                                             bool live) {
     uint32_t a[2][32];
     if (live) {
@@ -141,10 +147,9 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
         bits &= lim >= 32 ? 0xffffffffu : lim <= 0 ? 0u : (1u << lim) - 1u;
         if (r >= L) bits = 0u;
         uint32_t p[16];
-        const float4 *cf4 = reinterpret_cast<const float4 *>(colf + 32 * b);  // 16-byte aligned table
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-            const float4 c4 = cf4[g];
+            const float4 c4 = lds_f4(colf + (uint32_t)(32 * b + 4 * g) * 4u);  // 16-byte aligned table
             const int e = 2 * g;
             p[e] = pack_bf16x2(((bits >> (2 * e)) & 1u) ? __uint_as_float(a[bb][2 * e]) * c4.x : 0.f,
                                ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(a[bb][2 * e + 1]) * c4.y : 0.f);
@@ -347,7 +352,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         ++mma_phase;
         tc_fence_after();
     };
-    auto masked = [&](bool lower, const float *colf) {
+    auto masked = [&](bool lower, uint32_t colf) {
         // TMEM loads and stores are warp-collective: a warp takes part only if all its lanes are fine
         mask_scores(tmem + lane_base + kColScratch, r, L, lower, colf, half, __all_sync(0xffffffffu, ok) != 0);
         tc_fence_before();
@@ -363,7 +368,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 
     // P1 = (A^T)_ji kept for i >= j, times lambda^(i+1-L)
     wait_mma();
-    masked(false, wcol);
+    masked(false, sb + plan.wcol);
     if (tid == 0) {
         wait_mask();
         wait_load(B_LOAD2);
@@ -380,7 +385,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     }
     // P2 = (B^T)_ji kept for i >= j, times lambda^(i+1-L)
     wait_mma();
-    masked(false, wcol);
+    masked(false, sb + plan.wcol);
     if (tid == 0) {
         wait_mask();
         if (ok) {
@@ -399,7 +404,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     // A full chunk stages dV (over V) and dK (over Q) and starts their stores while mask 3 and MMA6 run,
     // so that only dQ is left once MMA6 is done.  One decision for the whole CTA (it has barriers).
     const bool early = __syncthreads_and(ok && L == kC) != 0;
-    masked(true, utab);
+    masked(true, sb + plan.utab);
     if (tid == 0) {
         wait_mask();
         wait_load(B_LOAD3);

@@ -162,9 +162,10 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
 }
 
 // Columns [c_begin, c_end) (multiples of 32) of row r of an accumulator at tcol, times f, as bf16 into a
-// staging tile laid out as the TMA box of the output: 64-column atoms of 128-byte rows with the 128B
-// swizzle (atom_cols 64), or 32-column atoms of 64-byte rows with the 64B swizzle (atom_cols 32).
-__device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end, float f, int r, uint8_t *tile,
+// staging tile at shared address `tile`, laid out as the TMA box of the output: 64-column atoms of 128-byte
+// rows with the 128B swizzle (atom_cols 64), or 32-column atoms of 64-byte rows with the 64B swizzle
+// (atom_cols 32).
+__device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end, float f, int r, uint32_t tile,
                                           int atom_cols) {
     for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         uint32_t a[32];
@@ -172,7 +173,7 @@ __device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end,
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint8_t *dst;
+            uint32_t dst;
             if (atom_cols == 64) {
                 const uint32_t phys = ((uint32_t)(((c0 & 63) >> 3) + q)) ^ ((uint32_t)r & 7u);
                 dst = tile + (uint32_t)(c0 >> 6) * 16384u + (uint32_t)r * 128u + (phys << 4);
@@ -180,11 +181,12 @@ __device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end,
                 const uint32_t phys = (uint32_t)q ^ (((uint32_t)r >> 1) & 3u);
                 dst = tile + (uint32_t)(c0 >> 5) * 8192u + (uint32_t)r * 64u + (phys << 4);
             }
-            *reinterpret_cast<uint4 *>(dst) =
-                make_uint4(pack_bf16x2(__uint_as_float(a[8 * q]) * f, __uint_as_float(a[8 * q + 1]) * f),
-                           pack_bf16x2(__uint_as_float(a[8 * q + 2]) * f, __uint_as_float(a[8 * q + 3]) * f),
-                           pack_bf16x2(__uint_as_float(a[8 * q + 4]) * f, __uint_as_float(a[8 * q + 5]) * f),
-                           pack_bf16x2(__uint_as_float(a[8 * q + 6]) * f, __uint_as_float(a[8 * q + 7]) * f));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q]) * f, __uint_as_float(a[8 * q + 1]) * f)),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 2]) * f, __uint_as_float(a[8 * q + 3]) * f)),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 4]) * f, __uint_as_float(a[8 * q + 5]) * f)),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 6]) * f, __uint_as_float(a[8 * q + 7]) * f))
+                         : "memory");
         }
     }
 }
@@ -423,10 +425,10 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         // and dK to the other
         const int vsplit = min(dv, 32 * ((dv + dk) / 64));
         if (half == 0) {
-            stage_row(tmem + lane_base + colDV, 0, vsplit, rf, r, smem + plan.v, 64);
+            stage_row(tmem + lane_base + colDV, 0, vsplit, rf, r, vb, 64);
         } else {
-            stage_row(tmem + lane_base + colDV, vsplit, dv, rf, r, smem + plan.v, 64);
-            stage_row(tmem + lane_base + colDK, 0, dk, rf, r, smem + plan.q, 32);
+            stage_row(tmem + lane_base + colDV, vsplit, dv, rf, r, vb, 64);
+            stage_row(tmem + lane_base + colDK, 0, dk, rf, r, qb, 32);
         }
         fence_async_shared();
         named_bar_sync(2, kThreads);
@@ -447,7 +449,7 @@ gla_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // atoms split between the halves, and written with one store per atom
             const int qsplit = 32 * ((nka + 1) / 2);
             stage_row(tmem + lane_base + colDQ, half == 0 ? 0 : qsplit, half == 0 ? qsplit : dk, qf, r,
-                      smem + plan.k, 32);
+                      kb, 32);
             fence_async_shared();
             named_bar_sync(2, kThreads);
             if (tid == 0) {

@@ -192,7 +192,8 @@ static_assert(B_COUNT <= 32, "the shared-memory plan reserves 32 barrier slots")
 // Output-gate factors in the tensor-core epilogue, which drains O on the chunk loop's critical path: two
 // gate values at a time in bf16 pairs, sigmoid(g) = (1 + tanh(g/2)) / 2 and SiLU(g) = g sigmoid(g) with the
 // hardware tanh approximation (one MUFU operation per pair).  The factors carry bf16 precision and an
-// absolute sigmoid error of a few 1e-3 at most, about the bf16 rounding of the output itself.
+// absolute sigmoid error of a few 1e-3 at most, about the bf16 rounding of the output itself; the drain
+// multiplies them by the row factor and by O rounded to bf16 in bf16 pairs as well.
 __device__ __forceinline__ uint32_t gate_factor_bf16x2(uint32_t g2, int kind) {
     const uint32_t half2 = 0x3f003f00u;  // (0.5, 0.5) in bf16
     uint32_t hg, t, f;
@@ -1010,6 +1011,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const int r = 32 * q4 + lane;                       // TMEM lane = token row
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
+        const uint32_t grow2 = pack_bf16x2(grow, grow);           // the same, as a bf16 pair (gated drain)
         uint8_t *xp = smem + o_xp + (uint32_t)q4 * 4096u;     // this warp's staging tile: 32 rows x 128 B
         bool ok = true;
         // O is free for the first chunk's MMA3 (the releases of O count toward SREADY, one phase later)
@@ -1152,10 +1154,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         uint32_t o2[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const uint32_t f2 = gate_factor_bf16x2(gw[e], gk);
-                            const float2 ff = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&f2));
-                            o2[e] = pack_bf16x2(__uint_as_float(x[2 * e]) * grow * ff.x,
-                                                __uint_as_float(x[2 * e + 1]) * grow * ff.y);
+                            // in bf16 pairs: the gate factor times the row factor, times O rounded to bf16
+                            uint32_t fg;
+                            asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(fg) : "r"(gate_factor_bf16x2(gw[e], gk)), "r"(grow2));
+                            asm("mul.rn.bf16x2 %0, %1, %2;"
+                                : "=r"(o2[e])
+                                : "r"(pack_bf16x2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]))), "r"(fg));
                         }
                         *cell = make_uint4(o2[0], o2[1], o2[2], o2[3]);
                     }

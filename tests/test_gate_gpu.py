@@ -84,9 +84,10 @@ def test_gated_prefill_segmented_long_sequence():
 
 
 def test_gated_prefill_leaves_the_state_and_matches_the_ungated_output():
-    """hT is bit-identical to the ungated forward's, and the gated output is the ungated output (before
-    its bf16 rounding) times the gate factor, so it agrees with the ungated output times the factor to
-    within two bf16 roundings."""
+    """hT is bit-identical to the ungated forward's, and the gated output is the ungated output times the gate
+    factor formed in bf16 pairs (O rounded to bf16, the factor times the row factor rounded to bf16, their
+    product rounded), so it agrees with the ungated output times the factor to within four bf16 roundings
+    (the reference's own output rounding included)."""
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=2, T=256, H=4, h0_std=0.02)
     d = I.make_prefill(w, device="cuda", seed=26)
     out_g, hT_g = check_gated_prefill(w, gla.GATE_SIGMOID, seed=26)
@@ -95,7 +96,7 @@ def test_gated_prefill_leaves_the_state_and_matches_the_ungated_output():
     assert torch.equal(hT, hT_g)
     g = I.make_gate(out.shape, device="cuda", seed=26)
     expect = out.float() * torch.sigmoid(g.float())
-    assert (out_g.float() - expect).abs().max().item() <= 2 ** -7 * expect.abs().max().item()
+    assert (out_g.float() - expect).abs().max().item() <= 2 ** -6 * expect.abs().max().item()
 
 
 @pytest.mark.parametrize("kind", KINDS)

@@ -105,6 +105,52 @@ __device__ __forceinline__ float silu_scaled(float z) { return silu(z); }
 template <>
 __device__ __forceinline__ float silu_scaled<__nv_bfloat16>(float hz) { return fmaf(hz, tanh_approx(hz), hz); }
 
+// Two f32 lanes per instruction: fma.rn.f32x2 rounds each lane as fma.rn.f32 does, so the paired
+// arithmetic below gives the scalar form's results bit for bit with half the FMA instructions.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// a bf16 pair (channels 2i, 2i+1 of one row) as an f32 pair
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+    return ((uint64_t)(w & 0xffff0000u) << 32) | (uint64_t)(w << 16);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+// One output row of a lane's 8 bf16 channels: z/2 = b/2 + sum_k (w_k/2) x_k in the order of the scalar
+// form, then hz + hz tanh(hz), as f32 pairs; x_k are the lane's 16 bytes of input rows t-3+k.
+__device__ __forceinline__ uint4 conv_row_bf16(const uint64_t (&w2)[4][4], const uint64_t (&b2)[4], const uint4 &x0,
+                                               const uint4 &x1, const uint4 &x2, const uint4 &x3) {
+    const uint32_t a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+    const uint32_t a2[4] = {x2.x, x2.y, x2.z, x2.w}, a3[4] = {x3.x, x3.y, x3.z, x3.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint64_t z = fma_f32x2(w2[0][p], bf16x2_to_f32x2(a0[p]), b2[p]);
+        z = fma_f32x2(w2[1][p], bf16x2_to_f32x2(a1[p]), z);
+        z = fma_f32x2(w2[2][p], bf16x2_to_f32x2(a2[p]), z);
+        z = fma_f32x2(w2[3][p], bf16x2_to_f32x2(a3[p]), z);
+        float zl, zh;
+        f32x2_split(z, zl, zh);
+        const uint64_t y = fma_f32x2(z, f32x2(tanh_approx(zl), tanh_approx(zh)), z);
+        float yl, yh;
+        f32x2_split(y, yl, yh);
+        o[p] = pack_bf16x2(yl, yh);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // sequence of `row` and its [start, end) rows; dense batches have cu == null
 __device__ __forceinline__ int seq_of(int64_t row, int nseq, int T, const int32_t *cu, int64_t &start,
                                       int64_t &end) {
@@ -236,27 +282,55 @@ conv_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const float *__rest
             if (!bad && r1 == r0 + kCvRun && start <= r0 - 3 && end >= r0 + kCvRun) {
                 // fast path: the run and its three inputs before lie inside one sequence; fully unrolled,
                 // so the window of the last four rows lives in registers without copies
-                float xw[kCvRun + 3][8];
-#pragma unroll
-                for (int m = 0; m < 3; ++m) row8(wbox + (size_t)m * row_bytes, lane, xw[m], (const T *)nullptr);
                 T *yp = y + (size_t)r0 * D + c0;
+                if constexpr (sizeof(T) == 2) {
+                    uint64_t w2[4][4], b2[4];
 #pragma unroll
-                for (int j = 0; j < kCvRun; ++j) {
-                    row8(wbox + (size_t)(j + 3) * row_bytes, lane, xw[j + 3], (const T *)nullptr);
-                    float out[8];
+                    for (int p = 0; p < 4; ++p) {
 #pragma unroll
-                    for (int e = 0; e < kVec; ++e) {
-                        const float z = fmaf(wt[3][e], xw[j + 3][e],
-                                             fmaf(wt[2][e], xw[j + 2][e], fmaf(wt[1][e], xw[j + 1][e], fmaf(wt[0][e], xw[j][e], bias[e]))));
-                        out[e] = silu_scaled<T>(z);
+                        for (int k = 0; k < 4; ++k) w2[k][p] = f32x2(wt[k][2 * p], wt[k][2 * p + 1]);
+                        b2[p] = f32x2(bias[2 * p], bias[2 * p + 1]);
                     }
-                    Vec8<T>::store(yp + (size_t)j * D, out);
-                }
-                if (end == r0 + kCvRun && st_out) {  // the run ends its sequence: the conv state
+                    uint4 xr[kCvRun + 3];  // the lane's 16 bytes of each staged row
 #pragma unroll
-                    for (int e = 0; e < kVec; ++e)
+                    for (int m = 0; m < 3; ++m) xr[m] = *reinterpret_cast<const uint4 *>(wbox + (size_t)m * row_bytes + 16 * lane);
 #pragma unroll
-                        for (int m = 0; m < 3; ++m) st_out[((size_t)s * D + c0 + e) * 3 + m] = xw[kCvRun + m][e];
+                    for (int j = 0; j < kCvRun; ++j) {
+                        xr[j + 3] = *reinterpret_cast<const uint4 *>(wbox + (size_t)(j + 3) * row_bytes + 16 * lane);
+                        __stcs(reinterpret_cast<uint4 *>(yp + (size_t)j * D),
+                               conv_row_bf16(w2, b2, xr[j], xr[j + 1], xr[j + 2], xr[j + 3]));
+                    }
+                    if (end == r0 + kCvRun && st_out) {  // the run ends its sequence: the conv state
+#pragma unroll
+                        for (int m = 0; m < 3; ++m) {
+                            float xm[8];
+                            Vec8<__nv_bfloat16>::unpack(xr[kCvRun + m], xm);
+#pragma unroll
+                            for (int e = 0; e < kVec; ++e) st_out[((size_t)s * D + c0 + e) * 3 + m] = xm[e];
+                        }
+                    }
+                } else {
+                    float xw[kCvRun + 3][8];
+#pragma unroll
+                    for (int m = 0; m < 3; ++m) row8(wbox + (size_t)m * row_bytes, lane, xw[m], (const T *)nullptr);
+#pragma unroll
+                    for (int j = 0; j < kCvRun; ++j) {
+                        row8(wbox + (size_t)(j + 3) * row_bytes, lane, xw[j + 3], (const T *)nullptr);
+                        float out[8];
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e) {
+                            const float z = fmaf(wt[3][e], xw[j + 3][e],
+                                                 fmaf(wt[2][e], xw[j + 2][e], fmaf(wt[1][e], xw[j + 1][e], fmaf(wt[0][e], xw[j][e], bias[e]))));
+                            out[e] = silu_scaled<T>(z);
+                        }
+                        Vec8<T>::store(yp + (size_t)j * D, out);
+                    }
+                    if (end == r0 + kCvRun && st_out) {  // the run ends its sequence: the conv state
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e)
+#pragma unroll
+                            for (int m = 0; m < 3; ++m) st_out[((size_t)s * D + c0 + e) * 3 + m] = xw[kCvRun + m][e];
+                    }
                 }
             } else if (!bad) {
                 float h[3][8];  // x_{t-3}, x_{t-2}, x_{t-1}

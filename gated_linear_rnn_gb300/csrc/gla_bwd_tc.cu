@@ -122,10 +122,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&p)[16
 // is reached by every thread (also when `live` is false: then the warp only passes it).  The kept
 // columns of each 32-column block are one 32-bit mask (bit t for column 32 b + t), so no per-element
 // comparison is kept live.
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
+// Four f32 values at a 16-byte aligned shared address, as two pairs (values 0, 1 and 2, 3).
+__device__ __forceinline__ void lds_f32x2x2(uint32_t addr, uint64_t &a, uint64_t &b) {
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+// Two f32 values (bit patterns) times the pair g2 with one instruction: mul.rn.f32x2 rounds each lane as
+// mul.rn.f32 does, so the results are those of two scalar multiplies.
+__device__ __forceinline__ void mul_f32x2(uint32_t &lo, uint32_t &hi, uint64_t g2) {
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%0, %1};\n\tmul.rn.f32x2 t, t, %2;\n\tmov.b64 {%0, %1}, t;\n\t}"
+        : "+r"(lo), "+r"(hi)
+        : "l"(g2));
+}
+__device__ __forceinline__ uint64_t f32x2_splat(float g) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(g));
+    return d;
 }
 
 __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool lower, uint32_t colf, int half,
@@ -149,12 +160,16 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
         uint32_t p[16];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-            const float4 c4 = lds_f4(colf + (uint32_t)(32 * b + 4 * g) * 4u);  // 16-byte aligned table
+            uint64_t c01, c23;  // column factors of columns 32 b + 4 g .. + 3 (16-byte aligned table)
+            lds_f32x2x2(colf + (uint32_t)(32 * b + 4 * g) * 4u, c01, c23);
             const int e = 2 * g;
-            p[e] = pack_bf16x2(((bits >> (2 * e)) & 1u) ? __uint_as_float(a[bb][2 * e]) * c4.x : 0.f,
-                               ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(a[bb][2 * e + 1]) * c4.y : 0.f);
-            p[e + 1] = pack_bf16x2(((bits >> (2 * e + 2)) & 1u) ? __uint_as_float(a[bb][2 * e + 2]) * c4.z : 0.f,
-                                   ((bits >> (2 * e + 3)) & 1u) ? __uint_as_float(a[bb][2 * e + 3]) * c4.w : 0.f);
+            uint32_t x0 = a[bb][2 * e], x1 = a[bb][2 * e + 1], x2 = a[bb][2 * e + 2], x3 = a[bb][2 * e + 3];
+            mul_f32x2(x0, x1, c01);
+            mul_f32x2(x2, x3, c23);
+            p[e] = pack_bf16x2(((bits >> (2 * e)) & 1u) ? __uint_as_float(x0) : 0.f,
+                               ((bits >> (2 * e + 1)) & 1u) ? __uint_as_float(x1) : 0.f);
+            p[e + 1] = pack_bf16x2(((bits >> (2 * e + 2)) & 1u) ? __uint_as_float(x2) : 0.f,
+                                   ((bits >> (2 * e + 3)) & 1u) ? __uint_as_float(x3) : 0.f);
         }
         tmem_st16(tbase + (uint32_t)(16 * b), p);
     }
@@ -167,10 +182,13 @@ __device__ __forceinline__ void mask_scores(uint32_t tbase, int r, int L, bool l
 // (atom_cols 32).
 __device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end, float f, int r, uint32_t tile,
                                           int atom_cols) {
+    const uint64_t f2 = f32x2_splat(f);
     for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         uint32_t a[32];
         tmem_ld32(tcol + (uint32_t)c0, a);
         tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) mul_f32x2(a[e], a[e + 1], f2);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t dst;
@@ -182,10 +200,10 @@ __device__ __forceinline__ void stage_row(uint32_t tcol, int c_begin, int c_end,
                 dst = tile + (uint32_t)(c0 >> 5) * 8192u + (uint32_t)r * 64u + (phys << 4);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                         "r"(pack_bf16x2(__uint_as_float(a[8 * q]) * f, __uint_as_float(a[8 * q + 1]) * f)),
-                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 2]) * f, __uint_as_float(a[8 * q + 3]) * f)),
-                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 4]) * f, __uint_as_float(a[8 * q + 5]) * f)),
-                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 6]) * f, __uint_as_float(a[8 * q + 7]) * f))
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q]), __uint_as_float(a[8 * q + 1]))),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 2]), __uint_as_float(a[8 * q + 3]))),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 4]), __uint_as_float(a[8 * q + 5]))),
+                         "r"(pack_bf16x2(__uint_as_float(a[8 * q + 6]), __uint_as_float(a[8 * q + 7])))
                          : "memory");
         }
     }

@@ -211,6 +211,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Two f32 values (bit patterns) times the pair g2 with one instruction: mul.rn.f32x2 rounds each lane as
+// mul.rn.f32 does, so the results are those of two scalar multiplies.
+__device__ __forceinline__ uint64_t f32x2_splat(float g) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(g));
+    return d;
+}
+__device__ __forceinline__ void mul_f32x2(uint32_t &lo, uint32_t &hi, uint64_t g2) {
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%0, %1};\n\tmul.rn.f32x2 t, t, %2;\n\tmov.b64 {%0, %1}, t;\n\t}"
+        : "+r"(lo), "+r"(hi)
+        : "l"(g2));
+}
+// 32 values in place, in pairs
+__device__ __forceinline__ void scale32(uint32_t (&v)[32], uint64_t g2) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) mul_f32x2(v[e], v[e + 1], g2);
+}
+
 // The four contractions as groups of K-steps of 16, fully unrolled, with every operand descriptor advanced
 // by a constant from a base computed once: the MMA warp spends a few instructions per tcgen05.mma, so the
 // tensor pipe is not left waiting for it to issue.  A descriptor holds its start address in 16-byte units,
@@ -691,7 +709,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 // state before the c-th chunk: lambda^walked * frame; at a block start the frame is
                 // brought back to the true state (TMEM rewritten) and walked restarts at 0
-                const float g = expf(ld * (float)walked);
+                const uint64_t g2 = f32x2_splat(expf(ld * (float)walked));
                 if (r < dk) {
                     for (int j0 = 0; j0 < dv; j0 += 64) {
                         uint32_t v[2][32];
@@ -699,11 +717,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
                             tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
                             tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * g);
-                                v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g);
-                            }
+                            scale32(v[0], g2);
+                            scale32(v[1], g2);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 32; ++e) {
@@ -801,14 +816,14 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 const bool last = c == nchunks - 1;
-                const float g = expf(ld * (float)(rows_before(c) + plen(c)));
+                const uint64_t g2 = f32x2_splat(expf(ld * (float)(rows_before(c) + plen(c))));
                 if (r < dk) {
                     for (int j0 = 0; j0 < dv; j0 += 32) {
                         uint32_t v[32];
                         tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * g);
+                        scale32(v, g2);
                         if (last) {
                             if (final_state) {
                                 float4 *dst = reinterpret_cast<float4 *>(final_state + (int64_t)r * dv + j0);
@@ -851,6 +866,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const float g_prev = (fact && c >= 1) ? tab[plen(c - 1)] : 1.f;
             const float g_copy = g_prev;
             const float g_tmem = fact ? g_prev : (last ? 1.f : tab[plen(c)]);
+            const uint64_t gc2 = f32x2_splat(g_copy);
             if (r < dk) {
                 // two 32-column groups per step: both TMEM loads in flight before the first use
                 for (int j0 = 0; j0 < dv; j0 += 64) {
@@ -870,11 +886,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             v[e >> 3][4 * (e & 7) + 3] = __float_as_uint(x.w);
                         }
                     }
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * g_copy);
-                        v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * g_copy);
-                    }
+                    scale32(v[0], gc2);
+                    scale32(v[1], gc2);
                     if (last) {
                         if (final_state) {
                             float4 *dst = reinterpret_cast<float4 *>(final_state + (int64_t)r * dv + j0);
@@ -899,12 +912,9 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                        pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
                     }
                     if (g_tmem != g_copy || c == 0) {
-                        const float gt = g_tmem / (c == 0 ? 1.f : g_copy);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            v[0][e] = __float_as_uint(__uint_as_float(v[0][e]) * gt);
-                            v[1][e] = __float_as_uint(__uint_as_float(v[1][e]) * gt);
-                        }
+                        const uint64_t gt2 = f32x2_splat(g_tmem / (c == 0 ? 1.f : g_copy));
+                        scale32(v[0], gt2);
+                        scale32(v[1], gt2);
                     }
                     tmem_st32(tmem + lane_base + kColS + (uint32_t)j0, v[0]);
                     tmem_st32(tmem + lane_base + kColS + (uint32_t)j0 + 32u, v[1]);
@@ -1012,6 +1022,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const float grow = fact ? tab[min(r + 1, kC)] : 1.f;  // lambda^(r+1): the factored row factor
         const uint32_t grow2 = pack_bf16x2(grow, grow);           // the same, as a bf16 pair (gated drain)
+        const uint64_t grow_f2 = f32x2_splat(grow);                // and as an f32 pair (ungated drain)
         uint8_t *xp = smem + o_xp + (uint32_t)q4 * 4096u;     // this warp's staging tile: 32 rows x 128 B
         bool ok = true;
         // O is free for the first chunk's MMA3 (the releases of O count toward SREADY, one phase later)
@@ -1031,6 +1042,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0, v[0]);
                 tmem_ld32(tmem + lane_base + kColO + (uint32_t)j0 + 32u, v[1]);
                 tmem_wait_ld();
+                scale32(v[0], grow_f2);
+                scale32(v[1], grow_f2);
                 if (j0 + 64 >= dv) {  // last TMEM read of O for this chunk: MMA3 of the next chunk may start
                     tc_fence_before();
                     __syncwarp();
@@ -1044,10 +1057,10 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 for (int q8 = 0; q8 < 8; ++q8) {
                     const uint32_t *x = &v[q8 >> 2][8 * (q8 & 3)];
                     *reinterpret_cast<uint4 *>(myrow + (((uint32_t)q8 ^ (uint32_t)(lane & 7)) << 4)) = make_uint4(
-                        pack_bf16x2(__uint_as_float(x[0]) * grow, __uint_as_float(x[1]) * grow),
-                        pack_bf16x2(__uint_as_float(x[2]) * grow, __uint_as_float(x[3]) * grow),
-                        pack_bf16x2(__uint_as_float(x[4]) * grow, __uint_as_float(x[5]) * grow),
-                        pack_bf16x2(__uint_as_float(x[6]) * grow, __uint_as_float(x[7]) * grow));
+                        pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                        pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                        pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                        pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
                 }
                 if (full) {
                     fence_async_shared();  // the staged rows must be visible to the TMA engine

@@ -265,13 +265,14 @@ __device__ __forceinline__ uint64_t desc_v(uint32_t a) { return smem_desc(a, 163
 __device__ __forceinline__ uint64_t desc_s(uint32_t a, int dk) { return smem_desc(a, (uint32_t)dk * 128u, 1024, kSwizzle128B); }
 
 // Multiply the 16-byte chunk at `p` (8 bf16) by f, in place.
-__device__ __forceinline__ void scale_chunk_bf16(uint8_t *p, float f) {
+__device__ __forceinline__ void scale_chunk_bf16(uint8_t *p, uint64_t f2) {
     uint4 x = *reinterpret_cast<uint4 *>(p);
     uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float2 fl = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[e]));
-        w[e] = pack_bf16x2(fl.x * f, fl.y * f);
+        uint32_t lo = w[e] << 16, hi = w[e] & 0xffff0000u;  // the bf16 pair as two f32 values
+        mul_f32x2(lo, hi, f2);
+        w[e] = pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
     }
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -282,10 +283,11 @@ __device__ __forceinline__ void scale_chunk_bf16(uint8_t *p, float f) {
 // over all banks: chunk i of thread r is physical chunk i ^ ((r >> 1) & 3).
 __device__ __forceinline__ void scale_row_sw64(uint8_t *tile, int nka, int r, float f) {
     const int x = (r >> 1) & 3;
+    const uint64_t f2 = f32x2_splat(f);
     for (int a = 0; a < nka; ++a) {
         uint8_t *row = tile + a * 8192 + r * 64;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) scale_chunk_bf16(row + ((i ^ x) << 4), f);
+        for (int i = 0; i < 4; ++i) scale_chunk_bf16(row + ((i ^ x) << 4), f2);
     }
 }
 

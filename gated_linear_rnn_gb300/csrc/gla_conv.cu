@@ -201,8 +201,10 @@ __device__ __forceinline__ void row8(const uint8_t *row, int lane, float (&x)[8]
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+// 104 registers: two CTAs of 288 threads per SM (59,904 of 65,536 registers) and no spills; a
+// two-CTA launch bound lets the compiler stop at 96 and spill inside the row loop.
 template <typename T>
-__global__ void __launch_bounds__(kCvThreads, 2)
+__global__ void __maxnreg__(104)
 conv_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const float *__restrict__ w, const float *__restrict__ b,
                     const float *__restrict__ st_in, float *__restrict__ st_out, T *__restrict__ y, int64_t rows,
                     int nseq, int Tlen, int D, int slab, const int32_t *__restrict__ cu, int64_t ntiles) {

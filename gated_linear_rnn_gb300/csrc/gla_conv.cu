@@ -188,7 +188,7 @@ constexpr int kCvSlab = 256;                    // channels per CTA (the TMA box
 constexpr uint64_t kCvWaitNs = 2000000000ull;   // 2 s per wait
 
 template <typename T> struct CvStages;
-template <> struct CvStages<__nv_bfloat16> { static constexpr int n = 3; };  // 3 x 33.5 KB, two CTAs per SM
+template <> struct CvStages<__nv_bfloat16> { static constexpr int n = 3; };  // 3 x 33.5 KB
 template <> struct CvStages<float> { static constexpr int n = 2; };          // 2 x 67 KB
 
 // 8 channels of one staged row (the lane's 16 bytes of bf16, or 32 bytes of f32)
@@ -201,8 +201,9 @@ __device__ __forceinline__ void row8(const uint8_t *row, int lane, float (&x)[8]
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// 104 registers: two CTAs of 288 threads per SM (59,904 of 65,536 registers) and no spills; a
-// two-CTA launch bound lets the compiler stop at 96 and spill inside the row loop.
+// 104 registers and no spills (a launch bound for two CTAs per SM makes the compiler stop at 96 and spill
+// inside the row loop).  One CTA then fits per SM: each of the SM's four sub-partitions holds 16 K
+// registers, and two CTAs of nine warps would put five warps on one of them.
 template <typename T>
 __global__ void __maxnreg__(104)
 conv_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const float *__restrict__ w, const float *__restrict__ b,
@@ -501,7 +502,9 @@ static int conv_prefill(const T *x, const float *w, const float *b, const float 
             cudaSuccess)
             return GLA_ERR_LAUNCH;
         // one wave: as many CTAs as the SMs hold at once (rounded down to whole slabs), each walking tiles
-        // t, t + gridDim.x, ...; a second partial wave would double the time of its tiles
+        // t, t + gridDim.x, ...; a second partial wave would double the time of its tiles.  At any moment the
+        // CTAs of all slabs read about the same rows, so DRAM sees whole rows of x (contiguous tile ranges
+        // per CTA over all SMs measured slower)
         const int per_sm = resident_ctas<T>(bytes);
         int64_t gx = (int64_t)per_sm * device_info().sm_count / nslabs;
         gx = gx < 1 ? 1 : gx;

@@ -398,18 +398,19 @@ __global__ void conv_empty_kernel(const float *__restrict__ st_in, float *__rest
         st_out[(size_t)s * D * 3 + e] = st_in ? st_in[(size_t)s * D * 3 + e] : 0.f;
 }
 
-// Step: a block owns 1024 channels (8 per thread) of kStepSeqs sequences, so the weights and bias
-// are read once per block and reused; two sequences' x and state are in flight at a time.
+// Step: a block owns 1024 channels (8 per thread) of spb consecutive sequences, so the weights and bias
+// are read once per block and reused; two sequences' x and state are in flight at a time.  The host
+// picks spb so that the grid is one wave (1280 sequences x 3072 channels: 9 a block, 429 blocks).
 constexpr int kStepThreads = 128;
-constexpr int kStepSeqs = 8;
+constexpr int kStepSeqs = 8;  // sequences per block when the occupancy cannot be looked up
 
 template <typename T>
 __global__ void __launch_bounds__(kStepThreads)
 conv_step_kernel(const T *__restrict__ x, const float *__restrict__ w, const float *__restrict__ b,
-                 float *__restrict__ state, T *__restrict__ y, int N, int D) {
+                 float *__restrict__ state, T *__restrict__ y, int N, int D, int spb) {
     const int c0 = (blockIdx.x * kStepThreads + threadIdx.x) * kVec;
     if (c0 >= D) return;
-    const int n0 = blockIdx.y * kStepSeqs;
+    const int n0 = blockIdx.y * spb, n1 = min(n0 + spb, N);
     float wt[4][8], bias[8];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
@@ -418,12 +419,12 @@ conv_step_kernel(const T *__restrict__ x, const float *__restrict__ w, const flo
         bias[i] = b ? __ldg(b + c0 + i) : 0.f;
     }
 #pragma unroll 1
-    for (int nn = 0; nn < kStepSeqs; nn += 2) {
+    for (int nn = n0; nn < n1; nn += 2) {
         float xt[2][8], hs[2][24];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int n = n0 + nn + u;
-            if (n >= N) continue;
+            const int n = nn + u;
+            if (n >= n1) continue;
             Vec8<T>::load(x + (size_t)n * D + c0, xt[u]);
             const float4 *sp = reinterpret_cast<const float4 *>(state + ((size_t)n * D + c0) * 3);  // 24 floats
 #pragma unroll
@@ -434,8 +435,8 @@ conv_step_kernel(const T *__restrict__ x, const float *__restrict__ w, const flo
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int n = n0 + nn + u;
-            if (n >= N) continue;
+            const int n = nn + u;
+            if (n >= n1) continue;
             float out[8];
 #pragma unroll
             for (int i = 0; i < kVec; ++i) {
@@ -532,15 +533,41 @@ int conv1d_silu_f32(const float *x, const float *w, const float *b, const float 
     return conv_prefill<float>(x, w, b, st_in, st_out, y, nseq, Tlen, D, cu, st);
 }
 
+// blocks of the step kernel the device holds at once (looked up once per device; 0 if that failed)
+static int step_resident_blocks() {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cache[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv_step_kernel<__nv_bfloat16>, kStepThreads, 0) !=
+            cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[dev].store(per_sm * device_info().sm_count, std::memory_order_relaxed);
+    return per_sm * device_info().sm_count;
+}
+
 int conv1d_silu_step_bf16(const void *x, const float *w, const float *b, float *state, void *y, int N, int D,
                           cudaStream_t st) {
     using B = __nv_bfloat16;
     const int cgroups = (D / kVec + kStepThreads - 1) / kStepThreads;
-    const int ngroups = (N + kStepSeqs - 1) / kStepSeqs;
     if (N <= 0) return GLA_OK;
+    // sequences per block: the fewest that keep the grid within one wave
+    const int resident = step_resident_blocks();
+    int spb = kStepSeqs;
+    if (resident > 0) {
+        const int64_t per_wave = resident / cgroups;  // blocks of sequences per wave
+        spb = per_wave > 0 ? (int)(((int64_t)N + per_wave - 1) / per_wave) : N;
+    }
+    const int ngroups = (N + spb - 1) / spb;
     if (ngroups > 65535) return GLA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)cgroups, (unsigned)ngroups);
-    conv_step_kernel<B><<<grid, kStepThreads, 0, st>>>((const B *)x, w, b, state, (B *)y, N, D);
+    conv_step_kernel<B><<<grid, kStepThreads, 0, st>>>((const B *)x, w, b, state, (B *)y, N, D, spb);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }

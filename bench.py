@@ -845,8 +845,8 @@ def run_e2e(args, P, D, w, wd, out, hT, dout, stream):
 
 def run_only(args):
     """W + K back-to-back calls of one operation (the backward of the layer workload, the conv over
-    B8 T2048 D3072, or the forward of a prefill workload), then a device-status check: a fixed command
-    line to put under a profiler."""
+    B8 T2048 D3072, the forward of a prefill workload, or the gated forward of the layer workload), then a
+    device-status check: a fixed command line to put under a profiler."""
     import torch
     from gated_linear_rnn_gb300 import build as Bld
     from gated_linear_rnn_gb300 import gla
@@ -858,16 +858,23 @@ def run_only(args):
     Bld.build_library()
     gla.load()
     w = I.WORKLOADS["layer_bf16"]
-    if args.only in ("layer", "long", "ragged"):
-        wp = I.WORKLOADS["layer_bf16" if args.only == "layer" else "long_bf16" if args.only == "long" else "ragged"]
+    if args.only in ("layer", "long", "ragged", "gated"):
+        wp = I.WORKLOADS["layer_bf16" if args.only in ("layer", "gated") else "long_bf16" if args.only == "long"
+                         else "ragged"]
         d = I.make_prefill(wp, device=dev, seed=0)
         cu = None if d["cu_seqlens"] is None else d["cu_seqlens"].to(dev)
         nseq = d["q"].shape[0] if cu is None else cu.numel() - 1
         out = torch.empty(d["q"].shape[:3] + (wp.dv,), dtype=torch.bfloat16, device=dev)
         hT = torch.empty(nseq, wp.H, wp.dk, wp.dv, dtype=torch.float32, device=dev)
 
+        g = I.make_gate(out.shape, device=dev, seed=5) if args.only == "gated" else None
+
         def call():
-            gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, hT, wp.chunk, cu)
+            if g is None:
+                gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["log_decay"], d["h0"], out, hT, wp.chunk, cu)
+            else:
+                gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], g, d["log_decay"], d["h0"], out, hT, wp.chunk, None,
+                                        gate_kind=gla.GATE_SILU)
     elif args.only == "backward":
         d = I.make_backward(w, device=dev, seed=0, dhT_std=0.0)
         dq, dk, dv = (torch.empty_like(d[k]) for k in ("q", "k", "v"))
@@ -899,10 +906,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd-steps", type=int, default=5, help="timed launches of the backward (0: skip)")
-    ap.add_argument("--only", choices=["backward", "conv", "layer", "long", "ragged"], default=None,
+    ap.add_argument("--only", choices=["backward", "conv", "layer", "long", "ragged", "gated"], default=None,
                     help="run just W + K calls of one operation on its bench workload (for profilers): the "
-                         "layer backward, the conv, or the forward of the layer, long-context or ragged "
-                         "workload; prints one status line, not the bench line")
+                         "layer backward, the conv, the forward of the layer, long-context or ragged "
+                         "workload, or the gated forward of the layer workload (SiLU gate); prints one status "
+                         "line, not the bench line")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of fp64 reference work to time")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -76,6 +76,20 @@ def test_conv_ragged_with_empty_sequences_and_tail_rows():
     assert np.array_equal(so.cpu().numpy(), so_ref)
 
 
+@pytest.mark.parametrize("N,D", [(1, 3072), (7, 3072), (151, 264), (1280, 3072), (3001, 3072)])
+def test_conv_step_batch_sizes(N, D):
+    """The step over batches that the launch splits into different numbers of sequences per block (one
+    block of one sequence up to many sequences a block): every sequence's output and state updated once."""
+    x, w, b, st = make((N, 1), D, torch.bfloat16, seed=N, nseq=N)
+    state = st.clone().cuda()
+    y = torch.empty(N, D, dtype=torch.bfloat16, device="cuda")
+    gla.gla_conv1d_silu_step(x[:, 0].contiguous().cuda(), w.cuda(), b.cuda(), state, y)
+    torch.cuda.synchronize()
+    y_ref, so_ref = oracle.conv1d_silu(x, w, b, st)
+    assert oracle.rel_err(y.float().cpu().numpy(), y_ref[:, 0]) <= 1e-2
+    assert np.array_equal(state.cpu().numpy(), so_ref)
+
+
 def test_conv_step_equals_one_token():
     N, D = 50, 3072
     x, w, b, st = make((N, 1), D, torch.bfloat16, seed=5, nseq=N)

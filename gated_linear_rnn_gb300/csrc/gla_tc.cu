@@ -382,6 +382,15 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (w > 0) init_state = P.seg_h0 + ((int64_t)chain * (P.nseg - 1) + w - 1) * sz_state;
         if (w < P.nseg - 1) final_state = nullptr;
     }
+    // The state warps read the initial state at their first state pass, a row per thread in 64-column
+    // groups, one after the other; in a walk over a whole chain (h0 from DRAM) its lines are asked into
+    // L2 here, before the barriers, tables and TMEM allocation, so that the later groups do not each wait
+    // for DRAM (ragged batch of 1,024 chains: 776 -> 768 us).  Segment start states come from the scan,
+    // which has just written them.
+    if (!segmented && init_state != nullptr && (int)threadIdx.x < P.dk) {
+        const char *row = reinterpret_cast<const char *>(init_state + (int64_t)threadIdx.x * P.dv);
+        for (int o = 0; o < P.dv * 4; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + o));
+    }
     const float ld = __ldg(P.log_decay + h);
     const float lam = expf(ld);
     // Factored decay: lambda^(i-j) = lambda^(i+1) * lambda^-(j+1).  K rows are scaled by lambda^-(j+1)

@@ -133,7 +133,7 @@ __host__ __device__ constexpr void smem_plan_tail(Smem &p, uint32_t at) {
     p.utab = p.tab + 132 * 4;
     p.bars = p.utab + 128 * 4;
     p.bars = (p.bars + 7u) & ~7u;
-    p.slot = p.bars + 32 * 8;  // room for up to 32 barriers
+    p.slot = p.bars + 40 * 8;  // room for up to 40 barriers
     p.abort = p.slot + 4;
     p.total = p.abort + 4;
 }
@@ -187,7 +187,8 @@ enum { B_QFULL = 0, B_QEMPTY, B_KVFULL0, B_KVFULL1, B_KVEMPTY0, B_KVEMPTY1, B_AF
 __device__ __forceinline__ int b_kvfull(int s) { return s == 0 ? B_KVFULL0 : s == 1 ? B_KVFULL1 : B_KVFULL2; }
 __device__ __forceinline__ int b_kvempty(int s) { return s == 0 ? B_KVEMPTY0 : s == 1 ? B_KVEMPTY1 : B_KVEMPTY2; }
 __device__ __forceinline__ int b_kprep(int s) { return s == 0 ? B_KPREP0 : s == 1 ? B_KPREP1 : B_KPREP2; }
-static_assert(B_COUNT <= 32, "the shared-memory plan reserves 32 barrier slots");
+// the gated instance's epilogue warps add two gate barriers each after B_COUNT
+static_assert(B_COUNT + 8 <= 40, "the shared-memory plan reserves 40 barrier slots");
 
 // Output-gate factors in the tensor-core epilogue, which drains O on the chunk loop's critical path: two
 // gate values at a time in bf16 pairs, sigmoid(g) = (1 + tanh(g/2)) / 2 and SiLU(g) = g sigmoid(g) with the
@@ -301,7 +302,7 @@ template <bool kRev, int kNst, bool kFull, bool kGate = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const Params P) {
+                    const __grid_constant__ CUtensorMap tmG, const Params P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 1024-aligned base, by pointer arithmetic on the shared array (not through an integer), so that
     // every access derived from it compiles to a shared-memory instruction
@@ -466,6 +467,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         // image store has too
         mbar_init(BAR(B_VEMPTY0), save_images ? 2 : 1);
         mbar_init(BAR(B_VEMPTY1), save_images ? 2 : 1);
+        if (kGate)  // gated drain: per epilogue warp, one barrier per gate buffer (TMA loads of 4 KB)
+            for (int i = 0; i < 8; ++i) mbar_init(BAR(B_COUNT + i), 1);
         fence_mbar_init();
     }
     if (threadIdx.x < kC + 4) tab[threadIdx.x] = (threadIdx.x <= kC) ? expf((float)threadIdx.x * ld) : 0.f;
@@ -488,6 +491,7 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             if (!state_only) tma_prefetch_desc(&tmO);
+            if (kGate) tma_prefetch_desc(&tmG);
             const uint32_t kvbytes = (uint32_t)nka * 8192u + (uint32_t)nva * 16384u;
             const uint32_t qbytes = (uint32_t)nka * 8192u;
             bool ok = true;
@@ -833,7 +837,6 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         uint32_t v[32];
                         tmem_ld32(tmem + lane_base + kColS + (uint32_t)j0, v);
                         tmem_wait_ld();
-#pragma unroll
                         scale32(v, g2);
                         if (last) {
                             if (final_state) {
@@ -1101,30 +1104,34 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         }
         // ---- gated instance: out = O * f(g).  The gate rows of a 64-column group (the warp's 32 rows x
-        // 128 bytes) are copied four rows per instruction (coalesced cp.async, no registers) into one of
-        // two 4 KB buffers, the gate buffer and the staging tile, alternating by group and laid out as the
-        // staging tile; each lane turns its own row of gate values into its row of gated output in place,
-        // and the group's TMA store goes out of that buffer.  The first two groups' gates are copied before
-        // O is ready, each later one as soon as the store two groups back has read its buffer; the next
-        // chunk's gate lines are prefetched into L2. ----
+        // 128 bytes) come in with one TMA box into one of two 4 KB buffers, the gate buffer and the staging
+        // tile, alternating by group and laid out as the staging tile (the box of the output store); each
+        // lane turns its own row of gate values into its row of gated output in place, and the group's TMA
+        // store goes out of that buffer.  The first two groups' gates are loaded before O is ready, each
+        // later one as soon as the store two groups back has read its buffer; the next chunk's gate lines
+        // are prefetched into L2.  Each buffer has its barrier (count 1, the box's bytes). ----
+        auto gbar = [&](int b) -> uint32_t { return BAR(B_COUNT + 2 * q4 + b); };
+        // gate loads per buffer, issued and waited for (scalars: a runtime index would put them in local memory)
+        uint32_t gissued0 = 0u, gissued1 = 0u, gused0 = 0u, gused1 = 0u;
+        auto wait_gate = [&](int b) -> bool {
+            const uint32_t n = b ? gused1 : gused0;
+            const bool landed = mbar_wait(gbar(b), n & 1u, abort_flag, kWaitBudgetNs);
+            if (b) ++gused1; else ++gused0;
+            return landed;
+        };
         for (int c = 0; c < nchunks && ok && kGate; ++c) {
             const int Lc = chunk_len(c);
             const int ng = dv / 64, gk = P.gate_kind;
             auto buf_of = [&](int j) -> uint32_t { return ((j & 1) ? o_xp : o_gb) + (uint32_t)q4 * 4096u; };
-            auto copy_gate = [&](int j) {
-                const uint32_t dst = sbase + buf_of(j);
-                const int rr0 = 32 * q4 + (lane >> 3);
-                const uint4 *gp = reinterpret_cast<const uint4 *>(
-                                      P.gate + ((row0 + (int64_t)c * kC + rr0) * H + h) * dv + 64 * j) + (lane & 7);
-                const int64_t step = (int64_t)H * dv / 2;  // four rows, in 16-byte units
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t row = 4u * (uint32_t)i + (uint32_t)(lane >> 3);
-                    const bool valid = rr0 + 4 * i < Lc;
-                    cp_async16(dst + row * 128u + ((((uint32_t)lane & 7u) ^ (row & 7u)) << 4),
-                               valid ? (const void *)(gp + i * step) : (const void *)P.gate, valid);
+            // the gate rows of group j (this warp's 32 rows x 64 columns) with one TMA box, laid out like the
+            // output staging; rows past the tensor read as zeros, rows of the next sequence are not stored
+            auto load_gate = [&](int j) {
+                if (lane == 0) {
+                    const uint32_t bar = gbar(j & 1);
+                    mbar_expect_tx(bar, 4096u);
+                    tma_load_2d(sbase + buf_of(j), &tmG, h * dv + 64 * j, row0 + c * kC + 32 * q4, bar);
                 }
-                cp_async_commit();
+                if (j & 1) ++gissued1; else ++gissued0;
             };
             if (c + 1 < nchunks && r < chunk_len(c + 1)) {
                 const __nv_bfloat16 *gn = P.gate + ((row0 + (int64_t)(c + 1) * kC + r) * H + h) * dv;
@@ -1133,8 +1140,8 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
             if (lane == 0) bulk_wait_read0();  // both buffers: the previous chunk's stores have read them
             __syncwarp();
-            copy_gate(0);
-            if (ng > 1) copy_gate(1);
+            load_gate(0);
+            if (ng > 1) load_gate(1);
             ok = mbar_wait(BAR(B_OFULL), c & 1, abort_flag, kWaitBudgetNs);
             if (!ok) break;
             tc_fence_after();
@@ -1148,17 +1155,13 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + kColO + (uint32_t)(j0 + 32 * hf), v);
                     if (hf == 0) {
-                        // gate j has landed (in the first group the copy of gate 1 may still be in flight)
-                        if (j == 0 && ng > 1)
-                            cp_async_wait_1();
-                        else
-                            cp_async_wait_all();
-                        __syncwarp();  // every lane's copies
+                        // gate j has landed
+                        ok = wait_gate(j & 1) && ok;
                         // the gate of group j + 1 goes where group j - 1 was staged, once that store has read it
                         if (j >= 1 && j + 1 < ng) {
                             if (lane == 0) bulk_wait_read0();
                             __syncwarp();
-                            copy_gate(j + 1);
+                            load_gate(j + 1);
                         }
                     }
                     tmem_wait_ld();
@@ -1215,6 +1218,12 @@ gla_tc_chunk_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         }
         if (lane == 0) bulk_wait_read0();  // no store may still read shared memory at exit
+        // no gate load may still be writing shared memory at exit (after a wait that gave up): bounded waits
+        // that do not end on the abort flag
+        if (kGate) {
+            for (; gused0 < gissued0; ++gused0) mbar_wait(gbar(0), gused0 & 1u, nullptr, kWaitBudgetNs);
+            for (; gused1 < gissued1; ++gused1) mbar_wait(gbar(1), gused1 & 1u, nullptr, kWaitBudgetNs);
+        }
         if (!ok) {
             record_status(GLA_ERR_TIMEOUT);
             *abort_flag = 1;
@@ -1382,28 +1391,29 @@ bool three_stages_fit(int dk, int dv) {
 
 template <bool kRev, int kNst, bool kFull, bool kGate = false>
 int launch_one(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
-               const Params &p, long long ctas, cudaStream_t st) {
+               const CUtensorMap &mg, const Params &p, long long ctas, cudaStream_t st) {
     const size_t bytes = (kFull ? smem_plan_full(p.dk, p.dv, kGate) : smem_plan(p.dk, p.dv)).total + 1024;  // + alignment slack
     if (cudaFuncSetAttribute(gla_tc_chunk_kernel<kRev, kNst, kFull, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)bytes) != cudaSuccess)
         return GLA_ERR_LAUNCH;
-    gla_tc_chunk_kernel<kRev, kNst, kFull, kGate><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, p);
+    gla_tc_chunk_kernel<kRev, kNst, kFull, kGate><<<(unsigned)ctas, kThreads, bytes, st>>>(mq, mk, mv, mo, mg, p);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH;
 }
 
+// mg: the output gate's map (gated passes; any valid map otherwise)
 int launch_tc(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
-              const Params &p, long long ctas, cudaStream_t st) {
+              const CUtensorMap &mg, const Params &p, long long ctas, cudaStream_t st) {
     if (ctas <= 0) return GLA_OK;
     if (ctas > 0x7fffffffLL) return GLA_ERR_UNSUPPORTED;
     if (p.mode == kWhole || p.mode == kSegmented)
-        return p.gate ? launch_one<false, 2, true, true>(mq, mk, mv, mo, p, ctas, st)
-                      : launch_one<false, 2, true, false>(mq, mk, mv, mo, p, ctas, st);
+        return p.gate ? launch_one<false, 2, true, true>(mq, mk, mv, mo, mg, p, ctas, st)
+                      : launch_one<false, 2, true, false>(mq, mk, mv, mo, mg, p, ctas, st);
     const bool three = p.mode == kStateOnly && three_stages_fit(p.dk, p.dv);
-    if (p.reverse && three) return launch_one<true, 3, false>(mq, mk, mv, mo, p, ctas, st);
-    if (p.reverse) return launch_one<true, 2, false>(mq, mk, mv, mo, p, ctas, st);
-    if (three) return launch_one<false, 3, false>(mq, mk, mv, mo, p, ctas, st);
-    return launch_one<false, 2, false>(mq, mk, mv, mo, p, ctas, st);
+    if (p.reverse && three) return launch_one<true, 3, false>(mq, mk, mv, mo, mg, p, ctas, st);
+    if (p.reverse) return launch_one<true, 2, false>(mq, mk, mv, mo, mg, p, ctas, st);
+    if (three) return launch_one<false, 3, false>(mq, mk, mv, mo, mg, p, ctas, st);
+    return launch_one<false, 2, false>(mq, mk, mv, mo, mg, p, ctas, st);
 }
 
 }  // namespace
@@ -1416,11 +1426,16 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (!tc_chunk_supported(dk, dv, kC)) return GLA_ERR_UNSUPPORTED;
     const uint64_t rows = cu ? (uint64_t)Tlen : (uint64_t)nseq * (uint64_t)Tlen;
     if (rows >= (1ull << 31)) return GLA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo, mg;
     if (!make_map(&mq, q, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mk, k, (uint64_t)H * dk, rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mv, v, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mo, out, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
+        return GLA_ERR_LAUNCH;
+    // the output gate, [rows, H, dv] like out: the same boxes, read by the gated drain
+    if (gate == nullptr)
+        mg = mo;
+    else if (!make_map(&mg, gate, (uint64_t)H * dv, rows, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
         return GLA_ERR_LAUNCH;
     Params p{};
     p.log_decay = ld;
@@ -1446,7 +1461,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     int seg_chunks = 0;
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
     p.lpt = (cu != nullptr && nseg == 1 && nseq > 1 && nseq <= kLptMaxSeq) ? 1 : 0;
-    if (nseg == 1) return launch_tc(mq, mk, mv, mo, p, chains, st);
+    if (nseg == 1) return launch_tc(mq, mk, mv, mo, mg, p, chains, st);
 
     // segmented schedule: stream-ordered scratch for the segment end / start states
     const size_t per = (size_t)chains * (size_t)(nseg - 1) * (size_t)dk * (size_t)dv;
@@ -1462,7 +1477,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
     p.chunk_states = nullptr;  // the end states from zero are not states of the sequence
-    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), st);
+    int rc = launch_tc(mq, mk, mv, mo, mg, p, chains * (nseg - 1), st);
     if (rc == GLA_OK) {
         dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
         gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg,
@@ -1474,7 +1489,7 @@ static int chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
         p.mode = kSegmented;
         p.grid_seg = nseg;
         p.chunk_states = reinterpret_cast<__nv_bfloat16 *>(images);
-        rc = launch_tc(mq, mk, mv, mo, p, chains * nseg, st);
+        rc = launch_tc(mq, mk, mv, mo, mg, p, chains * nseg, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
@@ -1535,7 +1550,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     const int nseg = plan_segments(nseq, H, Tlen, cu, &seg_chunks);
     p.lpt = (cu != nullptr && nseg == 1 && nseq > 1 && nseq <= kLptMaxSeq) ? 1 : 0;
     // the q and out maps are not read in a state-only pass
-    if (nseg == 1) return launch_tc(mk, mk, mv, mv, p, chains, st);
+    if (nseg == 1) return launch_tc(mk, mk, mv, mv, mv, p, chains, st);
 
     // few long chains: as the forward's segmented schedule, in walk order (backwards in time the first
     // walked segment is the sequence's last, which may be short): end states of walk segments
@@ -1552,7 +1567,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     p.seg_h0 = scratch + per;
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mk, mk, mv, mv, p, chains * (nseg - 1), st);
+    int rc = launch_tc(mk, mk, mv, mv, mv, p, chains * (nseg - 1), st);
     if (rc == GLA_OK) {
         const int seg_tokens = seg_chunks * kC;
         const int first_tokens = reverse ? Tlen - (nseg - 1) * seg_tokens : seg_tokens;
@@ -1565,7 +1580,7 @@ int tc_state_pass_bf16(const void *ka, const void *va, const float *ld, const fl
     if (rc == GLA_OK) {
         p.mode = kStates;
         p.grid_seg = nseg;
-        rc = launch_tc(mk, mk, mv, mv, p, chains * nseg, st);
+        rc = launch_tc(mk, mk, mv, mv, mv, p, chains * nseg, st);
     }
     cudaFreeAsync(scratch, st);
     return rc;
@@ -1655,7 +1670,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     p.seg_h0 = scratch + per;   // written in full by the scan before pass 2 reads it
     p.mode = kStateOnly;
     p.grid_seg = nseg - 1;
-    int rc = launch_tc(mq, mk, mv, mo, p, chains * (nseg - 1), st);
+    int rc = launch_tc(mq, mk, mv, mo, mo, p, chains * (nseg - 1), st);
     if (rc != GLA_OK) return rc;
     dim3 grid((unsigned)((dk * dv / 4 + 255) / 256), (unsigned)chains);
     gla_seg_scan_kernel<<<grid, 256, 0, st>>>(ld, h0, p.seg_end, scratch + per, H, dk, dv, nseg, seg_chunks * kC,
@@ -1664,7 +1679,7 @@ int tc_chunk_fwd_bf16_noalloc(const void *q, const void *k, const void *v, const
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     p.mode = kSegmented;
     p.grid_seg = nseg;
-    return launch_tc(mq, mk, mv, mo, p, chains * nseg, st);
+    return launch_tc(mq, mk, mv, mo, mo, p, chains * nseg, st);
 }
 
 }  // namespace gla

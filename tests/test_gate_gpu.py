@@ -58,10 +58,12 @@ def test_gated_prefill_tensor_cores(kind):
     check_gated_prefill(w, kind, seed=21)
 
 
-@pytest.mark.parametrize("dk,dv,chunk", [(48, 80, 128), (96, 192, 32), (96, 192, 64), (64, 64, 128)])
+@pytest.mark.parametrize("dk,dv,chunk", [(48, 80, 128), (96, 192, 32), (96, 192, 64), (64, 64, 128), (64, 128, 128),
+                                          (128, 128, 128)])
 def test_gated_prefill_other_shapes(dk, dv, chunk):
     """Head sizes and chunk lengths outside the tensor-core envelope (48 x 80, chunk 32) run the SIMT kernel;
-    chunk 64 runs on the tensor cores as two chunks per tile, (64, 64) on the tensor cores with other tiles."""
+    chunk 64 runs on the tensor cores as two chunks per tile, (64, 64) on the tensor cores with one 64-column
+    gate group per warp, (64, 128) and (128, 128) with two (the layer's dv 192 has three)."""
     w = I.scaled(I.WORKLOADS["layer_bf16"], B=1, T=260, H=2, dk=dk, dv=dv, h0_std=0.1)
     check_gated_prefill(w, gla.GATE_SILU, seed=22, chunk=chunk)
 
